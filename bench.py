@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark of the DCP top-K merge on one GB300 (or N independent replicas).
+
+One step = one dcp_topk_merge launch over the prefill-scale workload
+(T=8192 query rows, dcp=4 shards, K=2048 candidates per shard: 512 MiB of
+rank-major candidates in, 128 MiB of sorted winners out), inputs resident in
+HBM.  The timed region is bracketed by a barrier and a device synchronize;
+per-launch durations come from CUDA events on the launching stream.  Inputs
+(640 MiB) exceed the 129 MB L2, so no flush is needed between launches.
+
+Prints one JSON line (rank 0).  Besides the headline, the line carries the
+decode-size latencies (16 rows: the random and the tie-heavy workload) and the
+local-top-K + merge sweep, the HBM roofline of the merge kernel, the oracle
+timed on the host cores, and an end-to-end number through the Python API with
+host buffers.
+
+``--impl reference`` times the CPU oracle instead (the only reference this
+method has): a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "merge rows/s at K=2048, DCP=4 (prefill-scale merge, T=8192)"
+UNIT = "rows/s"
+WORKLOAD = ("prefill merge: T=8192 rows, dcp=4, K=2048 (8192 candidates/row), rank-major fp32 "
+            "scores bf16-rounded N(mu_t,1) with mu_t=(t mod 64)/8-4, distinct int32 ids per "
+            "shard range, row_starts=262144*(t//256), seed 4")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "merge_prefill_T8192_ncu.txt")
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def kernel_source_hash():
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_stable_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    try:
+        kv = {}
+        for line in open(PROFILE_SUMMARY):
+            if ":" in line and not line.startswith("#"):
+                k, _, v = line.partition(":")
+                kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_launches(torch, fn, steps, stream):
+    """Per-launch durations (ms) from CUDA events recorded on `stream`."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for k in range(steps):
+            fn()
+            evs[k + 1].record(stream)
+    return evs
+
+
+def durations(evs):
+    return [evs[k].elapsed_time(evs[k + 1]) for k in range(len(evs) - 1)]
+
+
+def median_of_reps(torch, fn, stream, reps=7, launches=200, graph=False):
+    """Median over `reps` repetitions of the mean per-launch time of
+    `launches` back-to-back launches (µs)."""
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(launches):
+                fn()
+        run = g.replay
+    else:
+        def run():
+            for _ in range(launches):
+                fn()
+    out = []
+    for _ in range(reps + 1):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            run()
+            b.record(stream)
+        b.synchronize()
+        out.append(a.elapsed_time(b) * 1000.0 / launches)
+    return statistics.median(out[1:])
+
+
+def cpu_oracle_sample(m, budget_s=10.0):
+    """The oracle as it stands, single-threaded, on rows of the workload until
+    about budget_s seconds have passed.  Returns (rows/s, rows, seconds)."""
+    import oracle
+
+    oracle.build()
+    rows_done, t0 = 0, time.perf_counter()
+    batch = 64
+    order = np.random.default_rng(0).permutation(m.T)
+    while True:
+        rows = order[rows_done % m.T: rows_done % m.T + batch]
+        oracle.merge(m.scores, m.ids, m.row_starts, rows=rows)
+        rows_done += len(rows)
+        el = time.perf_counter() - t0
+        if el >= budget_s or rows_done >= 4 * m.T:
+            return rows_done / el, rows_done, el
+
+
+def run_reference(args):
+    rank = env_int("RANK", 0)
+    if rank != 0:
+        return 0
+    m = workloads.prefill()
+    per_step = []
+    import oracle
+
+    oracle.build()
+    rng = np.random.default_rng(1)
+    # size each step's sample so the whole run stays within about two minutes
+    t0 = time.perf_counter()
+    oracle.merge(m.scores, m.ids, m.row_starts, rows=np.arange(16))
+    per_row = (time.perf_counter() - t0) / 16
+    sample_rows = int(max(1, min(256, 120.0 / (args.steps + args.warmup) / per_row)))
+    for k in range(args.warmup + args.steps):
+        rows = rng.choice(m.T, sample_rows, replace=False)
+        t0 = time.perf_counter()
+        oracle.merge(m.scores, m.ids, m.row_starts, rows=rows)
+        el = time.perf_counter() - t0
+        if k >= args.warmup:
+            per_step.append(el)
+    tot = sum(per_step)
+    value = sample_rows * len(per_step) / tot
+    sample = (f"{sample_rows} random rows of the prefill workload per step, single-threaded "
+              f"C oracle (qsort of 64-bit keys)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * tot / len(per_step), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    import sparse_attention_indexer_stable_gb300 as dk
+
+    world = env_int("WORLD_SIZE", 1)
+    rank = env_int("RANK", 0)
+    local_rank = env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist = dist_mod
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    m = workloads.prefill()
+    scores = torch.from_numpy(m.scores).to(dev)
+    ids = torch.from_numpy(m.ids).to(dev)
+    rs = torch.from_numpy(m.row_starts).to(dev)
+    out_ids = torch.empty((m.T, m.K), dtype=torch.int32, device=dev)
+    out_scores = torch.empty((m.T, m.K), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        dk.merge(scores, ids, rs, out_ids=out_ids, out_scores=out_scores, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t0 = time.perf_counter()
+        evs = time_launches(torch, step, args.steps, stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        barrier()
+        torch.cuda.synchronize(dev)
+    per = durations(evs)
+    total_ms = evs[0].elapsed_time(evs[-1])
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+    value = m.T * args.steps * world / (max_ms / 1000.0)
+
+    # roofline of the merge kernel (the only kernel of the step)
+    alg_bytes = m.algorithmic_bytes()
+    avg_launch_ms = statistics.mean(per)
+    achieved = alg_bytes / (avg_launch_ms / 1000.0) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # decode-size latencies and the local top-K + merge sweep (rank 0 only)
+    extras = {}
+    if rank == 0 and not args.skip_extras:
+        extras = decode_and_sweep(torch, dk, dev, stream)
+
+    # end to end through the Python API with host buffers
+    e2e = None
+    if not args.skip_extras:
+        e2e = end_to_end(torch, dk, m, dev, stream, steps=max(3, min(20, args.steps)))
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_extras:
+        v, rows, secs = cpu_oracle_sample(m, budget_s=args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{rows} rows of the prefill workload ({secs:.1f} s), single-threaded "
+                         f"C oracle"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": m.T, "dcp": m.dcp, "K": m.K,
+                       "chunk_rows": 1024, "l2": "inputs 640 MiB > 129 MB L2, no flush",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "us_per_launch": 1000.0 * avg_launch_ms,
+            "achieved_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": profiled_traffic(), "algorithmic_bytes": alg_bytes},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+            "wall_s_timed_region": wall,
+        }
+        line.update(extras)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def decode_and_sweep(torch, dk, dev, stream):
+    out = {}
+    for name in ("decode", "tieheavy"):
+        m = workloads.NAMED[name]()
+        s = torch.from_numpy(m.scores).to(dev)
+        i = torch.from_numpy(m.ids).to(dev)
+        oi = torch.empty((m.T, m.K), dtype=torch.int32, device=dev)
+        os_ = torch.empty((m.T, m.K), dtype=torch.float32, device=dev)
+
+        def fn():
+            dk.merge(s, i, out_ids=oi, out_scores=os_, stream=stream)
+
+        launch = median_of_reps(torch, fn, stream)
+        graph = median_of_reps(torch, fn, stream, graph=True)
+        out[f"{name}_T{m.T}_us_per_launch"] = launch
+        out[f"{name}_T{m.T}_us_per_graph_replay"] = graph
+    sweep = {}
+    K = 2048
+    for T in workloads.SWEEP_T:
+        logits = torch.from_numpy(workloads.sweep_logits(T)).to(dev)
+        dcp = logits.shape[0]
+        cs = torch.empty((dcp, T, K), dtype=torch.float32, device=dev)
+        ci = torch.empty((dcp, T, K), dtype=torch.int32, device=dev)
+        oi = torch.empty((T, K), dtype=torch.int32, device=dev)
+        os_ = torch.empty((T, K), dtype=torch.float32, device=dev)
+
+        def fn():
+            for r in range(dcp):
+                dk.local_topk(logits[r], K, r, dcp, out_scores=cs[r], out_ids=ci[r], stream=stream)
+            dk.merge(cs, ci, out_ids=oi, out_scores=os_, stream=stream)
+
+        sweep[str(T)] = {"us_per_step_launch": median_of_reps(torch, fn, stream, launches=50),
+                         "us_per_step_graph": median_of_reps(torch, fn, stream, launches=50,
+                                                             graph=True)}
+    out["sweep_local4_plus_merge"] = sweep
+    return out
+
+
+def end_to_end(torch, dk, m, dev, stream, steps):
+    """Same metric through the public API: every step copies the inputs from
+    pinned host memory, merges, and reads the result back to pinned host
+    memory, all inside the timed region."""
+    h_s = torch.from_numpy(m.scores).pin_memory()
+    h_i = torch.from_numpy(m.ids).pin_memory()
+    h_r = torch.from_numpy(m.row_starts).pin_memory()
+    h_oi = torch.empty((m.T, m.K), dtype=torch.int32).pin_memory()
+    h_os = torch.empty((m.T, m.K), dtype=torch.float32).pin_memory()
+    d_s = torch.empty_like(h_s, device=dev)
+    d_i = torch.empty_like(h_i, device=dev)
+    d_r = torch.empty_like(h_r, device=dev)
+    d_oi = torch.empty((m.T, m.K), dtype=torch.int32, device=dev)
+    d_os = torch.empty((m.T, m.K), dtype=torch.float32, device=dev)
+
+    def step():
+        d_s.copy_(h_s, non_blocking=True)
+        d_i.copy_(h_i, non_blocking=True)
+        d_r.copy_(h_r, non_blocking=True)
+        dk.merge(d_s, d_i, d_r, out_ids=d_oi, out_scores=d_os, stream=stream)
+        h_oi.copy_(d_oi, non_blocking=True)
+        h_os.copy_(d_os, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+    b.synchronize()
+    ms = a.elapsed_time(b)
+    h2d = h_s.numel() * 4 + h_i.numel() * 4 + h_r.numel() * 4
+    d2h = h_oi.numel() * 4 + h_os.numel() * 4
+    return {"value": m.T * steps / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="time only the headline step (used for profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

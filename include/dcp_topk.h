@@ -1,0 +1,134 @@
+/*
+ * dcp_topk.h -- C ABI of the GB300 (sm_103a) DCP sparse-indexer top-K library.
+ *
+ * Decode context parallelism (DCP) shards the KV cache across `dcp` ranks.
+ * Each rank keeps the top-K of its own shard's indexer logits; the merge then
+ * picks, per query row, the global top-K of the dcp*K gathered candidates
+ * ("[Kernel] Optimize CuTeDSL DCP top-k merge", Summary).  Here every shard
+ * lives in one GPU's memory, so no collective is involved.
+ *
+ * Selection order (all entry points): score descending, then lowest global
+ * token id; equivalently the 64-bit key (score_key(s) << 32) | ~id taken as
+ * unsigned, where score_key is the order-preserving map of the fp32 bits to
+ * u32 and ~id is the bitwise complement of the id as unsigned 32-bit
+ * ("[Kernel] Optimize CuTeDSL DCP top-k merge", Summary).  Consequences:
+ * +0.0 ranks above -0.0; among equal scores the smallest unsigned id wins,
+ * so a padding slot (score -inf, id -1) ranks below every real candidate.
+ * Output rows list the K winners in that order; scores are copied bit for bit.
+ * Results are deterministic: identical inputs give identical output bits.
+ * NaN scores are outside the contract.
+ *
+ * Conventions for every entry point:
+ *  - all data pointers are DEVICE pointers owned by the caller; the library
+ *    allocates nothing and keeps no pointer after the call returns;
+ *  - work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call does not synchronise, so results are ready only
+ *    when the stream reaches that point; calls issue no host-device sync and
+ *    may be captured in a CUDA graph once the device has been used by a
+ *    first (uncaptured) call of the same entry point;
+ *  - outputs must not overlap inputs;
+ *  - argument errors are reported before anything is enqueued.
+ */
+#ifndef DCP_TOPK_H
+#define DCP_TOPK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dcp_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    DCP_OK = 0,
+    DCP_ERR_INVALID = 1,     /* a null required pointer or an out-of-range size */
+    DCP_ERR_UNSUPPORTED = 2, /* valid, but beyond this build's limits (the caller may fall back) */
+    DCP_ERR_CUDA = 3         /* a CUDA runtime error while preparing or launching */
+} dcp_status;
+
+/* Compiled limits: K <= DCP_MAX_K, candidates per row (dcp*K, or L for the
+ * local top-K, or dcp*L for the fused top-K) <= DCP_MAX_CANDIDATES. */
+#define DCP_MAX_K 4096
+#define DCP_MAX_CANDIDATES 16384
+
+/*
+ * dcp_topk_merge -- global top-K of per-shard candidates.
+ *
+ * The merge of "[Kernel] Optimize CuTeDSL DCP top-k merge" (Summary), reading
+ * the gathered candidates in the rank-major layout of "Reserve the sparse
+ * indexer's DCP top-k merge scratch through the workspace manager" (Purpose)
+ * directly, without moving the rank dimension inside first.
+ *
+ *   scores      fp32 [dcp][T][K], rank-major: shard r's candidates for row t
+ *               start at scores + (r*T + t)*K.
+ *   ids         int32 [dcp][T][K], same layout; -1 marks a padding slot.
+ *   T, dcp, K   rows, shards, candidates per shard (= outputs per row).
+ *               T == 0 is a no-op returning DCP_OK.
+ *   row_starts  int32 [T] or NULL (all zero): added to every output id that is
+ *               not -1, per row (the per-row offsets of the second page,
+ *               Purpose).  The caller keeps id + row_starts[t] within int32.
+ *   out_ids     int32 [T][K] row-major.
+ *   out_scores  fp32  [T][K] row-major.
+ *   workspace   may be NULL: this build needs no scratch
+ *               (dcp_topk_merge_workspace_size reports 0 bytes).
+ *
+ * Errors: DCP_ERR_INVALID for T < 0, dcp < 1, K < 1, or a NULL scores, ids,
+ * out_ids or out_scores with T > 0; DCP_ERR_UNSUPPORTED for K > DCP_MAX_K,
+ * dcp*K > DCP_MAX_CANDIDATES, or a workspace smaller than the reported size;
+ * DCP_ERR_CUDA if the launch fails.
+ *
+ * Rows are independent; the rows are processed in chunks of 1024 by a
+ * persistent grid ("Reserve the sparse indexer's DCP top-k merge scratch
+ * through the workspace manager", Purpose), and the result does not depend
+ * on the chunking.
+ */
+dcp_status dcp_topk_merge(const float* scores, const int32_t* ids, int T, int dcp, int K,
+                          const int32_t* row_starts, int32_t* out_ids, float* out_scores,
+                          void* workspace, size_t workspace_bytes, dcp_stream_t stream);
+
+/*
+ * dcp_topk_merge_workspace_size -- scratch bytes dcp_topk_merge needs for
+ * these sizes (the merge reserved its scratch through a workspace manager in
+ * "Reserve the sparse indexer's DCP top-k merge scratch through the workspace
+ * manager", Purpose).  Writes 0: this build keeps every intermediate on chip.
+ * Errors as dcp_topk_merge's size checks; `bytes` must not be NULL.
+ */
+dcp_status dcp_topk_merge_workspace_size(int T, int dcp, int K, size_t* bytes);
+
+/*
+ * dcp_local_topk -- one rank's top-K over its own shard of indexer logits,
+ * the per-rank step before the merge ("[Kernel] Optimize CuTeDSL DCP top-k
+ * merge", Summary: each rank holds the local top-K of its 1/DCP KV shard).
+ *
+ *   logits      fp32 [T][ld], row-major; the first L columns of a row are this
+ *               rank's L local KV positions.
+ *   T, L, ld    rows, local columns, row stride in elements (ld >= L).
+ *   K           outputs per row; if L < K the row is padded with (-inf, -1).
+ *   rank, dcp   this rank and the number of shards (0 <= rank < dcp).
+ *   row_starts  int32 [T] or NULL (all zero).
+ *   out_scores  fp32  [T][K] row-major: this rank's slice of the rank-major
+ *               candidate buffer dcp_topk_merge reads (scores + rank*T*K).
+ *   out_ids     int32 [T][K]: global ids row_starts[t] + rank*L + column.
+ *
+ * Contiguous shards are this library's reading of the global id (the pages do
+ * not fix it): shard r owns local positions [r*L, (r+1)*L).  row_starts should
+ * be given to either this call or the merge, not both.
+ *
+ * Errors: DCP_ERR_INVALID for T < 0, L < 1, ld < L, K < 1, dcp < 1, rank out of
+ * range, or a NULL logits/out pointer with T > 0; DCP_ERR_UNSUPPORTED for
+ * K > DCP_MAX_K or L > DCP_MAX_CANDIDATES; DCP_ERR_CUDA if the launch fails.
+ */
+dcp_status dcp_local_topk(const float* logits, int T, int L, int ld, int K, int rank, int dcp,
+                          const int32_t* row_starts, float* out_scores, int32_t* out_ids,
+                          dcp_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* dcp_status_string(dcp_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCP_TOPK_H */

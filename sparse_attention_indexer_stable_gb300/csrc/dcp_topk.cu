@@ -1,0 +1,258 @@
+// dcp_topk.cu -- kernels and C ABI of the DCP top-K library (sm_103a).
+//
+// Entry points are declared and documented in include/dcp_topk.h.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "dcp_topk.h"
+#include "topk_core.cuh"
+
+namespace dcp {
+
+// Rows are walked 1024 at a time, as the merge of "Reserve the sparse
+// indexer's DCP top-k merge scratch through the workspace manager" (Purpose)
+// does; rows are independent, so this only fixes the order of the walk.
+constexpr int kChunkRows = 1024;
+
+struct MergeSource {
+  const float* scores;
+  const int32_t* ids;
+  const int32_t* row_starts;
+  int T, dcp, K;
+  bool vec4;
+
+  __device__ int count() const { return dcp * K; }
+
+  // Candidates of row t, rank-major: index i = r*K + k.
+  __device__ void stage(int t, uint32_t* skey, uint32_t* sinv) const {
+    const int n = dcp * K;
+    if (vec4) {
+      const int k4 = K >> 2;
+      for (int q = threadIdx.x; q < (n >> 2); q += kThreads) {
+        const int r = q / k4;
+        const int kk = (q - r * k4) << 2;
+        const size_t off = ((size_t)r * T + t) * (size_t)K + kk;
+        const uint4 sb = __ldg(reinterpret_cast<const uint4*>(scores + off));
+        const int4 ib = __ldg(reinterpret_cast<const int4*>(ids + off));
+        const int i = r * K + kk;
+        *reinterpret_cast<uint4*>(skey + i) =
+            make_uint4(score_key(sb.x), score_key(sb.y), score_key(sb.z), score_key(sb.w));
+        *reinterpret_cast<uint4*>(sinv + i) =
+            make_uint4(~(uint32_t)ib.x, ~(uint32_t)ib.y, ~(uint32_t)ib.z, ~(uint32_t)ib.w);
+      }
+    } else {
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int r = i / K;
+        const int k = i - r * K;
+        const size_t off = ((size_t)r * T + t) * (size_t)K + k;
+        skey[i] = score_key(__float_as_uint(__ldg(scores + off)));
+        sinv[i] = ~(uint32_t)__ldg(ids + off);
+      }
+    }
+  }
+
+  __device__ int32_t out_id(int t, uint32_t inv) const {
+    const uint32_t id = ~inv;
+    if (id == 0xFFFFFFFFu) return -1;
+    const uint32_t rs = row_starts ? (uint32_t)__ldg(row_starts + t) : 0u;
+    return (int32_t)(id + rs);
+  }
+};
+
+struct LocalSource {
+  const float* logits;
+  const int32_t* row_starts;
+  int L, ld, rank;
+  bool vec4;
+
+  __device__ int count() const { return L; }
+
+  __device__ void stage(int t, uint32_t* skey, uint32_t* sinv) const {
+    const float* row = logits + (size_t)t * (size_t)ld;
+    if (vec4) {
+      for (int q = threadIdx.x; q < (L >> 2); q += kThreads) {
+        const uint4 sb = __ldg(reinterpret_cast<const uint4*>(row) + q);
+        const int c = q << 2;
+        *reinterpret_cast<uint4*>(skey + c) =
+            make_uint4(score_key(sb.x), score_key(sb.y), score_key(sb.z), score_key(sb.w));
+        *reinterpret_cast<uint4*>(sinv + c) =
+            make_uint4(~(uint32_t)c, ~(uint32_t)(c + 1), ~(uint32_t)(c + 2), ~(uint32_t)(c + 3));
+      }
+    } else {
+      for (int c = threadIdx.x; c < L; c += kThreads) {
+        skey[c] = score_key(__float_as_uint(__ldg(row + c)));
+        sinv[c] = ~(uint32_t)c;
+      }
+    }
+  }
+
+  __device__ int32_t out_id(int t, uint32_t inv) const {
+    const uint32_t c = ~inv;
+    const uint32_t base = (row_starts ? (uint32_t)__ldg(row_starts + t) : 0u) +
+                          (uint32_t)rank * (uint32_t)L;
+    return (int32_t)(base + c);
+  }
+};
+
+__host__ __device__ inline int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+// Dynamic shared memory: SelectShared | win[n_pow2] (u64) | skey[n] | sinv[n],
+// each part 16-byte aligned.
+__host__ __device__ inline size_t row_smem_bytes(int n, int k) {
+  const int ksel = k < n ? k : n;
+  return align16(sizeof(SelectShared)) + align16((size_t)next_pow2(ksel) * 8) +
+         2 * align16((size_t)n * 4);
+}
+
+template <class Source>
+__global__ void __launch_bounds__(kThreads, 1)
+    topk_rows_kernel(Source src, int T, int K, float* __restrict__ out_scores,
+                     int32_t* __restrict__ out_ids) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SelectShared& s = *reinterpret_cast<SelectShared*>(smem_raw);
+  const int n = src.count();
+  const int ksel = K < n ? K : n;
+  const int n_pow2 = next_pow2(ksel);
+  unsigned char* p = smem_raw + align16(sizeof(SelectShared));
+  unsigned long long* win = reinterpret_cast<unsigned long long*>(p);
+  p += align16((size_t)n_pow2 * 8);
+  uint32_t* skey = reinterpret_cast<uint32_t*>(p);
+  p += align16((size_t)n * 4);
+  uint32_t* sinv = reinterpret_cast<uint32_t*>(p);
+
+  const int grid = (int)gridDim.x;
+  const int b = (int)blockIdx.x;
+  for (int cs = 0; cs < T; cs += kChunkRows) {
+    const int ce = min(T, cs + kChunkRows);
+    // first row of this chunk owned by this CTA: t == b (mod grid)
+    int t = cs + (((b - cs) % grid) + grid) % grid;
+    for (; t < ce; t += grid) {
+      src.stage(t, skey, sinv);
+      __syncthreads();
+      select_sort_row(s, skey, sinv, n, ksel, win, n_pow2);
+      float* os = out_scores + (size_t)t * (size_t)K;
+      int32_t* oi = out_ids + (size_t)t * (size_t)K;
+      for (int j = threadIdx.x; j < K; j += kThreads) {
+        if (j < ksel) {
+          const unsigned long long w = win[j];
+          os[j] = __uint_as_float(score_bits((uint32_t)(w >> 32)));
+          oi[j] = src.out_id(t, (uint32_t)w);
+        } else {
+          os[j] = __uint_as_float(0xFF800000u);  // -inf
+          oi[j] = -1;
+        }
+      }
+      // The next row's staging overwrites skey/sinv/win.
+      __syncthreads();
+    }
+  }
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int max_smem_optin = 0;
+  bool configured = false;
+};
+
+static DeviceInfo g_dev[64];
+static std::mutex g_dev_mutex;
+
+// Per-device launch limits and kernel attributes, set once per device (the
+// first call on a device must therefore not be inside a stream capture).
+static cudaError_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.configured) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    const int smem = d.max_smem_optin;
+    e = cudaFuncSetAttribute(topk_rows_kernel<MergeSource>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_rows_kernel<LocalSource>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    d.configured = true;
+  }
+  *out = &d;
+  return cudaSuccess;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+template <class Source>
+static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out_scores,
+                              int32_t* out_ids, cudaStream_t stream) {
+  DeviceInfo* d = nullptr;
+  if (device_info(&d) != cudaSuccess) return DCP_ERR_CUDA;
+  const size_t smem = row_smem_bytes(n, K);
+  if (smem > (size_t)d->max_smem_optin) return DCP_ERR_UNSUPPORTED;
+  const int grid = T < d->sms ? T : d->sms;
+  topk_rows_kernel<Source><<<grid, kThreads, smem, stream>>>(src, T, K, out_scores, out_ids);
+  return cudaGetLastError() == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
+}  // namespace dcp
+
+extern "C" {
+
+dcp_status dcp_topk_merge_workspace_size(int T, int dcp_, int K, size_t* bytes) {
+  if (!bytes || T < 0 || dcp_ < 1 || K < 1) return DCP_ERR_INVALID;
+  if (K > DCP_MAX_K || (long long)dcp_ * K > DCP_MAX_CANDIDATES) return DCP_ERR_UNSUPPORTED;
+  *bytes = 0;
+  return DCP_OK;
+}
+
+dcp_status dcp_topk_merge(const float* scores, const int32_t* ids, int T, int dcp_, int K,
+                          const int32_t* row_starts, int32_t* out_ids, float* out_scores,
+                          void* workspace, size_t workspace_bytes, dcp_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (T < 0 || dcp_ < 1 || K < 1) return DCP_ERR_INVALID;
+  if (K > DCP_MAX_K || (long long)dcp_ * K > DCP_MAX_CANDIDATES) return DCP_ERR_UNSUPPORTED;
+  if (T == 0) return DCP_OK;
+  if (!scores || !ids || !out_ids || !out_scores) return DCP_ERR_INVALID;
+  dcp::MergeSource src{scores, ids, row_starts, T, dcp_, K,
+                       (K % 4) == 0 && dcp::aligned16(scores) && dcp::aligned16(ids)};
+  return dcp::launch_rows(src, T, dcp_ * K, K, out_scores, out_ids, (cudaStream_t)stream);
+}
+
+dcp_status dcp_local_topk(const float* logits, int T, int L, int ld, int K, int rank, int dcp_,
+                          const int32_t* row_starts, float* out_scores, int32_t* out_ids,
+                          dcp_stream_t stream) {
+  if (T < 0 || L < 1 || ld < L || K < 1 || dcp_ < 1 || rank < 0 || rank >= dcp_)
+    return DCP_ERR_INVALID;
+  if (K > DCP_MAX_K || L > DCP_MAX_CANDIDATES) return DCP_ERR_UNSUPPORTED;
+  if (T == 0) return DCP_OK;
+  if (!logits || !out_scores || !out_ids) return DCP_ERR_INVALID;
+  dcp::LocalSource src{logits, row_starts, L, ld, rank,
+                       (L % 4) == 0 && (ld % 4) == 0 && dcp::aligned16(logits)};
+  return dcp::launch_rows(src, T, L, K, out_scores, out_ids, (cudaStream_t)stream);
+}
+
+const char* dcp_status_string(dcp_status status) {
+  switch (status) {
+    case DCP_OK: return "DCP_OK";
+    case DCP_ERR_INVALID: return "DCP_ERR_INVALID";
+    case DCP_ERR_UNSUPPORTED: return "DCP_ERR_UNSUPPORTED";
+    case DCP_ERR_CUDA: return "DCP_ERR_CUDA";
+  }
+  return "DCP_UNKNOWN_STATUS";
+}
+
+}  // extern "C"

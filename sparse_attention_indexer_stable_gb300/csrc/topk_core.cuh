@@ -1,0 +1,232 @@
+// topk_core.cuh -- per-row stable top-K selection on sm_103a.
+//
+// One CTA owns one query row at a time: the row's candidates sit in shared
+// memory as (32-bit score key, inverted id) pairs, and the CTA
+//   1. radix-selects the K-th largest score key with 11/11/10-bit digit
+//      histograms ("[Kernel] Optimize CuTeDSL DCP top-k merge", Summary: a
+//      radix pass over 32-bit score keys first),
+//   2. only if that threshold is shared by more candidates than there are
+//      slots left, radix-selects among the tied candidates on the inverted id
+//      (same page: the token-id tie-break pass runs only when the score
+//      threshold actually ties),
+//   3. compacts the K winners as 64-bit keys score_key<<32 | ~id,
+//   4. sorts them descending (score descending, then lowest id),
+//   5. writes scores (bit-exact, recovered from the key) and ids.
+//
+// Barrier discipline: every phase that reads a shared result (threshold digit,
+// counts) is separated by __syncthreads() from the next phase that resets or
+// rewrites that shared state.  The review of the same page reports the bug
+// this prevents: without a barrier between loading the threshold and zeroing
+// it, late warps read 0 and drop every tied candidate.
+#pragma once
+
+#include <cstdint>
+
+namespace dcp {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+constexpr int kHistBins = 2048;
+
+// Order-preserving map of fp32 bits to u32: unsigned order of the result is
+// float order, with -0.0 just below +0.0 and NaNs outside the finite range.
+__device__ __forceinline__ uint32_t score_key(uint32_t bits) {
+  return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+}
+
+// Inverse of score_key: the original fp32 bits.
+__device__ __forceinline__ uint32_t score_bits(uint32_t key) {
+  return (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
+}
+
+struct SelectShared {
+  uint32_t hist[kHistBins];
+  uint32_t warp_sum[kWarps];
+  uint32_t warp_off[kWarps];
+  uint32_t found_digit;
+  uint32_t found_above;
+  uint32_t found_count;
+  uint32_t win_count;
+  uint32_t dup_claim;
+};
+
+__device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t u = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
+// Finds the digit d of the histogram with above(d) < need <= above(d) + hist[d],
+// above(d) = sum of hist[e] for e > d.  nbins <= 2 * kThreads.  Exactly one
+// thread writes found_*; the caller must __syncthreads() before reading them.
+__device__ __forceinline__ void find_threshold_digit(SelectShared& s, int nbins, uint32_t need) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int b0 = nbins - 1 - 2 * tid;
+  const int b1 = b0 - 1;
+  const uint32_t h0 = b0 >= 0 ? s.hist[b0] : 0u;
+  const uint32_t h1 = b1 >= 0 ? s.hist[b1] : 0u;
+  const uint32_t local = h0 + h1;
+  const uint32_t incl = warp_inclusive_scan(local);
+  if (lane == 31) s.warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = s.warp_sum[lane];
+    const uint32_t wi = warp_inclusive_scan(w);
+    s.warp_off[lane] = wi - w;
+  }
+  __syncthreads();
+  const uint32_t excl = s.warp_off[warp] + incl - local;
+  if (h0 != 0u && excl < need && need <= excl + h0) {
+    s.found_digit = (uint32_t)b0;
+    s.found_above = excl;
+    s.found_count = h0;
+  } else if (h1 != 0u && excl + h0 < need && need <= excl + local) {
+    s.found_digit = (uint32_t)b1;
+    s.found_above = excl + h0;
+    s.found_count = h1;
+  }
+}
+
+// Result of a radix select over one 32-bit value per participating candidate.
+// The selected ones are those with (v & mask) > prefix, plus `need` of those
+// with (v & mask) == prefix (which number `count`).  If need == count they all
+// are; otherwise mask == ~0u and the `count` candidates are exact duplicates
+// of the value `prefix`.
+struct RadixResult {
+  uint32_t mask;
+  uint32_t prefix;
+  uint32_t need;
+  uint32_t count;
+};
+
+// Radix select of the `need` largest values (1 <= need <= participants).
+// ValueFn(i, v) -> bool: whether candidate i participates, and its value.
+template <class ValueFn>
+__device__ __forceinline__ RadixResult radix_select(SelectShared& s, int n, uint32_t need,
+                                                    ValueFn value) {
+  const int tid = threadIdx.x;
+  RadixResult r{0u, 0u, need, 0u};
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int nbins = pass == 2 ? 1024 : 2048;
+    const uint32_t dmask = (uint32_t)nbins - 1u;
+    for (int b = tid; b < nbins; b += kThreads) s.hist[b] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+      uint32_t v;
+      if (value(i, v) && (v & r.mask) == r.prefix) atomicAdd(&s.hist[(v >> shift) & dmask], 1u);
+    }
+    __syncthreads();
+    find_threshold_digit(s, nbins, r.need);
+    __syncthreads();
+    const uint32_t d = s.found_digit, above = s.found_above, cnt = s.found_count;
+    r.need -= above;
+    r.prefix |= d << shift;
+    r.mask |= dmask << shift;
+    r.count = cnt;
+    // Every thread has now read found_* and the histogram; only after this
+    // barrier may the next pass (or the caller) reset them.
+    __syncthreads();
+    if (cnt == r.need) break;
+  }
+  return r;
+}
+
+// Bitonic sort of n_pow2 64-bit keys in shared memory, descending.
+__device__ __forceinline__ void bitonic_sort_desc(unsigned long long* a, int n_pow2) {
+  const int tid = threadIdx.x;
+  for (int k = 2; k <= n_pow2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < (n_pow2 >> 1); i += kThreads) {
+        const int lo = 2 * i - (i & (j - 1));
+        const int hi = lo + j;
+        const unsigned long long x = a[lo], y = a[hi];
+        const bool desc = (lo & k) == 0;
+        if (desc ? (x < y) : (x > y)) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// The whole per-row selection.  skey/sinv hold the row's n candidates; on
+// return win[0..ksel) holds the winners sorted descending by 64-bit key.
+// n_pow2: a power of two >= ksel; win must have room for n_pow2 keys.
+__device__ __forceinline__ void select_sort_row(SelectShared& s, const uint32_t* skey,
+                                                const uint32_t* sinv, int n, int ksel,
+                                                unsigned long long* win, int n_pow2) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+
+  // 1. Threshold on the 32-bit score key.
+  const RadixResult rs = radix_select(s, n, (uint32_t)ksel, [&](int i, uint32_t& v) {
+    v = skey[i];
+    return true;
+  });
+
+  // 2. Tie-break on the inverted id, only when the threshold key ties beyond
+  //    the remaining slots.
+  const bool tie = rs.need != rs.count;
+  RadixResult rt{0u, 0u, 0u, 0u};
+  if (tie) {
+    const uint32_t tau = rs.prefix;
+    rt = radix_select(s, n, rs.need, [&](int i, uint32_t& v) {
+      v = sinv[i];
+      return skey[i] == tau;
+    });
+  }
+  const bool dup = tie && rt.need != rt.count;
+  if (tid == 0) {
+    s.win_count = 0u;
+    s.dup_claim = 0u;
+  }
+  __syncthreads();
+
+  // 3. Compaction of the winners (order is irrelevant: the sort below fixes
+  //    it, and candidates with equal 64-bit keys are identical).
+  for (int base = 0; base < n; base += kThreads) {
+    const int i = base + tid;
+    bool w = false;
+    uint32_t k = 0u, inv = 0u;
+    if (i < n) {
+      k = skey[i];
+      inv = sinv[i];
+      const uint32_t km = k & rs.mask;
+      if (km > rs.prefix) {
+        w = true;
+      } else if (km == rs.prefix) {
+        if (!tie) {
+          w = true;
+        } else {
+          const uint32_t um = inv & rt.mask;
+          if (um > rt.prefix) w = true;
+          else if (um == rt.prefix) w = !dup || atomicAdd(&s.dup_claim, 1u) < rt.need;
+        }
+      }
+    }
+    const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, w);
+    uint32_t slot0 = 0u;
+    if (lane == 0 && ballot) slot0 = atomicAdd(&s.win_count, (uint32_t)__popc(ballot));
+    slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
+    if (w) {
+      const uint32_t slot = slot0 + (uint32_t)__popc(ballot & ((1u << lane) - 1u));
+      if (slot < (uint32_t)n_pow2) win[slot] = ((unsigned long long)k << 32) | inv;
+    }
+  }
+  for (int j = ksel + tid; j < n_pow2; j += kThreads) win[j] = 0ull;
+  __syncthreads();
+
+  // 4. Final order.
+  bitonic_sort_desc(win, n_pow2);
+}
+
+}  // namespace dcp
