@@ -9,6 +9,7 @@
 
 #include "dcp_topk.h"
 #include "topk_core.cuh"
+#include "topk_fast.cuh"
 
 namespace dcp {
 
@@ -54,6 +55,27 @@ struct MergeSource {
     }
   }
 
+  // Fast path staging: the row's scores, then its ids, as 16-byte copies
+  // straight from the rank-major layout (needs K % 4 == 0 and 16-byte
+  // aligned bases).
+  __device__ int staged_words() const { return 2 * dcp * K; }
+
+  __device__ void issue(int t, uint32_t* dst) const {
+    const int k4 = K >> 2;
+    const int c4 = dcp * k4;
+    for (int c = threadIdx.x; c < 2 * c4; c += kThreads) {
+      const int plane = c >= c4;  // 0: scores, 1: ids
+      const int cc = c - plane * c4;
+      const int r = cc / k4;
+      const int kk = (cc - r * k4) << 2;
+      const size_t off = ((size_t)r * T + t) * (size_t)K + kk;
+      const void* g = plane ? (const void*)(ids + off) : (const void*)(scores + off);
+      cp_async16(dst + plane * (dcp * K) + r * K + kk, g);
+    }
+  }
+
+  __device__ uint32_t inv(const uint32_t* buf, int i) const { return ~buf[dcp * K + i]; }
+
   __device__ int32_t out_id(int t, uint32_t inv) const {
     const uint32_t id = ~inv;
     if (id == 0xFFFFFFFFu) return -1;
@@ -88,6 +110,15 @@ struct LocalSource {
       }
     }
   }
+
+  __device__ int staged_words() const { return L; }
+
+  __device__ void issue(int t, uint32_t* dst) const {
+    const float* row = logits + (size_t)t * (size_t)ld;
+    for (int c = threadIdx.x; c < (L >> 2); c += kThreads) cp_async16(dst + 4 * c, row + 4 * c);
+  }
+
+  __device__ uint32_t inv(const uint32_t*, int i) const { return ~(uint32_t)i; }
 
   __device__ int32_t out_id(int t, uint32_t inv) const {
     const uint32_t c = ~inv;
@@ -138,7 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (; t < ce; t += grid) {
       src.stage(t, skey, sinv);
       __syncthreads();
-      select_sort_row(s, skey, sinv, n, ksel, win, n_pow2);
+      select_sort_row(s, n, ksel, win, n_pow2, [&](int i) { return skey[i]; },
+                      [&](int i) { return sinv[i]; });
       float* os = out_scores + (size_t)t * (size_t)K;
       int32_t* oi = out_ids + (size_t)t * (size_t)K;
       for (int j = threadIdx.x; j < K; j += kThreads) {
@@ -187,6 +219,12 @@ static cudaError_t device_info(DeviceInfo** out) {
     e = cudaFuncSetAttribute(topk_rows_kernel<LocalSource>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_fast_kernel<MergeSource>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_fast_kernel<LocalSource>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
     d.configured = true;
   }
   *out = &d;
@@ -195,15 +233,23 @@ static cudaError_t device_info(DeviceInfo** out) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Streaming path when the row fits it (n <= 8192, K <= 2048, 16-byte copies
+// possible); the general path otherwise.
 template <class Source>
-static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out_scores,
-                              int32_t* out_ids, cudaStream_t stream) {
+static dcp_status launch_rows(const Source& src, int T, int n, int staged_words, int K,
+                              float* out_scores, int32_t* out_ids, cudaStream_t stream) {
   DeviceInfo* d = nullptr;
   if (device_info(&d) != cudaSuccess) return DCP_ERR_CUDA;
-  const size_t smem = row_smem_bytes(n, K);
-  if (smem > (size_t)d->max_smem_optin) return DCP_ERR_UNSUPPORTED;
   const int grid = T < d->sms ? T : d->sms;
-  topk_rows_kernel<Source><<<grid, kThreads, smem, stream>>>(src, T, K, out_scores, out_ids);
+  const size_t fast_smem = fast_smem_bytes(staged_words);
+  if (src.vec4 && n <= kFastMaxN && K <= kFastMaxK && fast_smem <= (size_t)d->max_smem_optin) {
+    topk_fast_kernel<Source><<<grid, kThreads, fast_smem, stream>>>(src, T, K, out_scores,
+                                                                     out_ids);
+  } else {
+    const size_t smem = row_smem_bytes(n, K);
+    if (smem > (size_t)d->max_smem_optin) return DCP_ERR_UNSUPPORTED;
+    topk_rows_kernel<Source><<<grid, kThreads, smem, stream>>>(src, T, K, out_scores, out_ids);
+  }
   return cudaGetLastError() == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
 }
 
@@ -229,7 +275,8 @@ dcp_status dcp_topk_merge(const float* scores, const int32_t* ids, int T, int dc
   if (!scores || !ids || !out_ids || !out_scores) return DCP_ERR_INVALID;
   dcp::MergeSource src{scores, ids, row_starts, T, dcp_, K,
                        (K % 4) == 0 && dcp::aligned16(scores) && dcp::aligned16(ids)};
-  return dcp::launch_rows(src, T, dcp_ * K, K, out_scores, out_ids, (cudaStream_t)stream);
+  return dcp::launch_rows(src, T, dcp_ * K, 2 * dcp_ * K, K, out_scores, out_ids,
+                          (cudaStream_t)stream);
 }
 
 dcp_status dcp_local_topk(const float* logits, int T, int L, int ld, int K, int rank, int dcp_,
@@ -242,7 +289,7 @@ dcp_status dcp_local_topk(const float* logits, int T, int L, int ld, int K, int 
   if (!logits || !out_scores || !out_ids) return DCP_ERR_INVALID;
   dcp::LocalSource src{logits, row_starts, L, ld, rank,
                        (L % 4) == 0 && (ld % 4) == 0 && dcp::aligned16(logits)};
-  return dcp::launch_rows(src, T, L, K, out_scores, out_ids, (cudaStream_t)stream);
+  return dcp::launch_rows(src, T, L, L, K, out_scores, out_ids, (cudaStream_t)stream);
 }
 
 const char* dcp_status_string(dcp_status status) {

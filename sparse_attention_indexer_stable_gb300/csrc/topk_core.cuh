@@ -158,18 +158,20 @@ __device__ __forceinline__ void bitonic_sort_desc(unsigned long long* a, int n_p
   }
 }
 
-// The whole per-row selection.  skey/sinv hold the row's n candidates; on
-// return win[0..ksel) holds the winners sorted descending by 64-bit key.
+// The whole per-row selection over n candidates given by accessors:
+// key(i) -> 32-bit score key, inv(i) -> inverted id.  On return
+// win[0..ksel) holds the winners sorted descending by 64-bit key.
 // n_pow2: a power of two >= ksel; win must have room for n_pow2 keys.
-__device__ __forceinline__ void select_sort_row(SelectShared& s, const uint32_t* skey,
-                                                const uint32_t* sinv, int n, int ksel,
-                                                unsigned long long* win, int n_pow2) {
+template <class KeyFn, class InvFn>
+__device__ __forceinline__ void select_sort_row(SelectShared& s, int n, int ksel,
+                                                unsigned long long* win, int n_pow2,
+                                                KeyFn key, InvFn inv) {
   const int tid = threadIdx.x;
   const int lane = tid & 31;
 
   // 1. Threshold on the 32-bit score key.
   const RadixResult rs = radix_select(s, n, (uint32_t)ksel, [&](int i, uint32_t& v) {
-    v = skey[i];
+    v = key(i);
     return true;
   });
 
@@ -180,8 +182,8 @@ __device__ __forceinline__ void select_sort_row(SelectShared& s, const uint32_t*
   if (tie) {
     const uint32_t tau = rs.prefix;
     rt = radix_select(s, n, rs.need, [&](int i, uint32_t& v) {
-      v = sinv[i];
-      return skey[i] == tau;
+      v = inv(i);
+      return key(i) == tau;
     });
   }
   const bool dup = tie && rt.need != rt.count;
@@ -196,10 +198,10 @@ __device__ __forceinline__ void select_sort_row(SelectShared& s, const uint32_t*
   for (int base = 0; base < n; base += kThreads) {
     const int i = base + tid;
     bool w = false;
-    uint32_t k = 0u, inv = 0u;
+    uint32_t k = 0u, u = 0u;
     if (i < n) {
-      k = skey[i];
-      inv = sinv[i];
+      k = key(i);
+      u = inv(i);
       const uint32_t km = k & rs.mask;
       if (km > rs.prefix) {
         w = true;
@@ -207,7 +209,7 @@ __device__ __forceinline__ void select_sort_row(SelectShared& s, const uint32_t*
         if (!tie) {
           w = true;
         } else {
-          const uint32_t um = inv & rt.mask;
+          const uint32_t um = u & rt.mask;
           if (um > rt.prefix) w = true;
           else if (um == rt.prefix) w = !dup || atomicAdd(&s.dup_claim, 1u) < rt.need;
         }
@@ -219,7 +221,7 @@ __device__ __forceinline__ void select_sort_row(SelectShared& s, const uint32_t*
     slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
     if (w) {
       const uint32_t slot = slot0 + (uint32_t)__popc(ballot & ((1u << lane) - 1u));
-      if (slot < (uint32_t)n_pow2) win[slot] = ((unsigned long long)k << 32) | inv;
+      if (slot < (uint32_t)n_pow2) win[slot] = ((unsigned long long)k << 32) | u;
     }
   }
   for (int j = ksel + tid; j < n_pow2; j += kThreads) win[j] = 0ull;

@@ -101,6 +101,13 @@ CASES = [
     (4, 5, 999, "wide", 0.0),
     (3, 4, 2048, "const", 0.5),
     (200, 4, 2048, "bf16", 0.0),
+    (5, 4, 2048, "cluster", 0.0),
+    (3, 2, 1024, "cluster", 0.1),
+    (300, 4, 2048, "ties", 0.02),
+    (160, 3, 2048, "zeros", 0.0),
+    (4, 4, 2048, "neginf", 0.0),
+    (4, 4, 2048, "wide", 0.0),
+    (2, 2, 2, "cluster", 0.0),
 ]
 
 

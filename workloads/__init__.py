@@ -134,7 +134,8 @@ def random_merge(seed: int, T: int, dcp: int, K: int, mode: str = "normal",
     mode: ``normal`` (fp32 N(0,1)), ``bf16`` (N(0,1) rounded to bf16),
     ``ties`` (4 distinct values), ``const`` (one value), ``zeros`` (+0/-0 and
     a few +-1), ``neginf`` (many real -inf scores), ``wide`` (ids spread over
-    the whole non-negative int32 range).
+    the whole non-negative int32 range), ``cluster`` (most top scores within a
+    few ulps of each other).
     pad_frac: fraction of slots, anywhere in each shard, replaced by padding.
     """
     rng = np.random.default_rng(seed)
@@ -157,6 +158,23 @@ def random_merge(seed: int, T: int, dcp: int, K: int, mode: str = "normal",
         scores = np.full(shape, 0.5, np.float32)
     elif mode == "zeros":
         scores = np.array([0.0, -0.0, 1.0, -1.0, 0.0, -0.0], np.float32)[rng.integers(0, 6, shape)]
+    elif mode == "cluster":
+        # most of each row's top candidates packed into a few ulps above 1.0,
+        # plus one candidate at 1.2 in the same top-11-bit bin: keys that
+        # agree on every bit but the lowest few, the hardest case for
+        # bucketing on leading bits
+        scores = rng.uniform(-1.0, 0.5, size=shape).astype(np.float32)
+        n = dcp * K
+        m = max(1, (3 * min(n, 4096)) // 8 + K // 2)
+        m = min(m, n - 1) if n > 1 else 1
+        base = np.uint32(np.float32(1.0).view(np.uint32))
+        flat = scores.transpose(1, 0, 2).reshape(T, n)
+        for t in range(T):
+            pos = rng.choice(n, min(n, m + 1), replace=False)
+            flat[t, pos[:m]] = (base + rng.choice(4096, m, replace=m > 4096).astype(np.uint32)).view(np.float32)
+            if len(pos) > m:
+                flat[t, pos[m]] = np.float32(1.2)
+        scores = np.ascontiguousarray(flat.reshape(T, dcp, K).transpose(1, 0, 2))
     elif mode == "neginf":
         scores = np.where(rng.random(shape) < 0.6, NEG_INF,
                           rng.standard_normal(shape, dtype=np.float32)).astype(np.float32)
