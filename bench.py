@@ -266,7 +266,7 @@ def run_ours(args):
         if dist is not None:
             dist.barrier()
 
-    m = workloads.prefill()
+    m = workloads.NAMED[args.workload]()
     scores = torch.from_numpy(m.scores).to(dev)
     ids = torch.from_numpy(m.ids).to(dev)
     rs = torch.from_numpy(m.row_starts).to(dev)
@@ -326,7 +326,8 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "T": m.T, "dcp": m.dcp, "K": m.K,
+            "config": {"workload": WORKLOAD if args.workload == "prefill" else args.workload,
+                       "T": m.T, "dcp": m.dcp, "K": m.K,
                        "chunk_rows": 1024, "l2": "inputs 640 MiB > 129 MB L2, no flush",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "us_per_launch": 1000.0 * avg_launch_ms,
@@ -436,6 +437,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-extras", action="store_true",
                     help="time only the headline step (used for profiling runs)")
+    ap.add_argument("--workload", default="prefill", choices=sorted(workloads.NAMED),
+                    help="the merge workload of the headline step (default: prefill)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

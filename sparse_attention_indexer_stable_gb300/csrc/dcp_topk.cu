@@ -58,23 +58,60 @@ struct MergeSource {
   // Fast path staging: the row's scores, then its ids, as 16-byte copies
   // straight from the rank-major layout (needs K % 4 == 0 and 16-byte
   // aligned bases).
-  __device__ int staged_words() const { return 2 * dcp * K; }
+  __host__ __device__ int staged_words() const { return 2 * dcp * K; }
 
+  template <int NT>
   __device__ void issue(int t, uint32_t* dst) const {
-    const int k4 = K >> 2;
-    const int c4 = dcp * k4;
-    for (int c = threadIdx.x; c < 2 * c4; c += kThreads) {
-      const int plane = c >= c4;  // 0: scores, 1: ids
-      const int cc = c - plane * c4;
-      const int r = cc / k4;
-      const int kk = (cc - r * k4) << 2;
-      const size_t off = ((size_t)r * T + t) * (size_t)K + kk;
-      const void* g = plane ? (const void*)(ids + off) : (const void*)(scores + off);
-      cp_async16(dst + plane * (dcp * K) + r * K + kk, g);
+    const int n = dcp * K;
+    const size_t stride = (size_t)T * (size_t)K;
+    const float* sp = scores + (size_t)t * (size_t)K;
+    const int32_t* ip = ids + (size_t)t * (size_t)K;
+    for (int r = 0; r < dcp; ++r, sp += stride, ip += stride) {
+      for (int kk = 4 * (int)threadIdx.x; kk < K; kk += 4 * NT) {
+        cp_async16(dst + r * K + kk, sp + kk);
+        cp_async16(dst + n + r * K + kk, ip + kk);
+      }
     }
   }
 
   __device__ uint32_t inv(const uint32_t* buf, int i) const { return ~buf[dcp * K + i]; }
+
+  // Inverted ids of staged candidates 4c .. 4c+3.
+  __device__ uint4 inv4(const uint32_t* buf, int c) const {
+    const uint4 w = *reinterpret_cast<const uint4*>(buf + dcp * K + 4 * c);
+    return make_uint4(~w.x, ~w.y, ~w.z, ~w.w);
+  }
+
+  // Starts pulling row t's candidates into L2 (one thread; no completion to
+  // wait for: the later 16-byte copies of the row then hit L2).
+  __device__ void prefetch_l2(int t) const {
+    const size_t stride = (size_t)T * (size_t)K;
+    const size_t off = (size_t)t * (size_t)K;
+    for (int r = 0; r < dcp; ++r) {
+      prefetch_l2_bulk(scores + off + r * stride, (uint32_t)K * 4u);
+      prefetch_l2_bulk(ids + off + r * stride, (uint32_t)K * 4u);
+    }
+  }
+
+  // Candidate i of row t read from global memory (the fallback path).
+  __device__ uint32_t key_global(int t, int i) const {
+    const int r = i / K;
+    return score_key(__float_as_uint(__ldg(scores + ((size_t)r * T + t) * (size_t)K + (i - r * K))));
+  }
+  __device__ uint32_t inv_global(int t, int i) const {
+    const int r = i / K;
+    return ~(uint32_t)__ldg(ids + ((size_t)r * T + t) * (size_t)K + (i - r * K));
+  }
+
+  // Per-row part of the output id, read once per row.
+  __device__ uint32_t row_base(int t) const {
+    return row_starts ? (uint32_t)__ldg(row_starts + t) : 0u;
+  }
+
+  __device__ int32_t out_id_from(uint32_t base, uint32_t inv) const {
+    const uint32_t id = ~inv;
+    return id == 0xFFFFFFFFu ? -1 : (int32_t)(id + base);
+  }
 
   __device__ int32_t out_id(int t, uint32_t inv) const {
     const uint32_t id = ~inv;
@@ -111,14 +148,37 @@ struct LocalSource {
     }
   }
 
-  __device__ int staged_words() const { return L; }
+  __host__ __device__ int staged_words() const { return L; }
 
+  template <int NT>
   __device__ void issue(int t, uint32_t* dst) const {
     const float* row = logits + (size_t)t * (size_t)ld;
-    for (int c = threadIdx.x; c < (L >> 2); c += kThreads) cp_async16(dst + 4 * c, row + 4 * c);
+    for (int c = threadIdx.x; c < (L >> 2); c += NT) cp_async16(dst + 4 * c, row + 4 * c);
   }
 
   __device__ uint32_t inv(const uint32_t*, int i) const { return ~(uint32_t)i; }
+
+  __device__ uint4 inv4(const uint32_t*, int c) const {
+    const uint32_t i = 4u * (uint32_t)c;
+    return make_uint4(~i, ~(i + 1u), ~(i + 2u), ~(i + 3u));
+  }
+
+  __device__ uint32_t row_base(int t) const {
+    return (row_starts ? (uint32_t)__ldg(row_starts + t) : 0u) + (uint32_t)rank * (uint32_t)L;
+  }
+
+  __device__ void prefetch_l2(int t) const {
+    prefetch_l2_bulk(logits + (size_t)t * (size_t)ld, (uint32_t)L * 4u);
+  }
+
+  __device__ uint32_t key_global(int t, int i) const {
+    return score_key(__float_as_uint(__ldg(logits + (size_t)t * (size_t)ld + i)));
+  }
+  __device__ uint32_t inv_global(int, int i) const { return ~(uint32_t)i; }
+
+  __device__ int32_t out_id_from(uint32_t base, uint32_t inv) const {
+    return (int32_t)(base + ~inv);
+  }
 
   __device__ int32_t out_id(int t, uint32_t inv) const {
     const uint32_t c = ~inv;
@@ -169,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (; t < ce; t += grid) {
       src.stage(t, skey, sinv);
       __syncthreads();
-      select_sort_row(s, n, ksel, win, n_pow2, [&](int i) { return skey[i]; },
-                      [&](int i) { return sinv[i]; });
+      select_sort_row<kThreads>(s, n, ksel, win, n_pow2, [&](int i) { return skey[i]; },
+                                [&](int i) { return sinv[i]; });
       float* os = out_scores + (size_t)t * (size_t)K;
       int32_t* oi = out_ids + (size_t)t * (size_t)K;
       for (int j = threadIdx.x; j < K; j += kThreads) {
@@ -198,6 +258,14 @@ struct DeviceInfo {
 static DeviceInfo g_dev[64];
 static std::mutex g_dev_mutex;
 
+template <class K>
+static cudaError_t allow_max_smem(K kernel, int bytes) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
 // Per-device launch limits and kernel attributes, set once per device (the
 // first call on a device must therefore not be inside a stream capture).
 static cudaError_t device_info(DeviceInfo** out) {
@@ -213,18 +281,12 @@ static cudaError_t device_info(DeviceInfo** out) {
     e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
     const int smem = d.max_smem_optin;
-    e = cudaFuncSetAttribute(topk_rows_kernel<MergeSource>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_rows_kernel<LocalSource>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_fast_kernel<MergeSource>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_fast_kernel<LocalSource>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    if ((e = allow_max_smem(topk_rows_kernel<MergeSource>, smem)) != cudaSuccess) return e;
+    if ((e = allow_max_smem(topk_rows_kernel<LocalSource>, smem)) != cudaSuccess) return e;
+    if ((e = allow_max_smem(topk_stream_kernel<512, MergeSource>, smem)) != cudaSuccess) return e;
+    if ((e = allow_max_smem(topk_stream_kernel<1024, MergeSource>, smem)) != cudaSuccess) return e;
+    if ((e = allow_max_smem(topk_stream_kernel<512, LocalSource>, smem)) != cudaSuccess) return e;
+    if ((e = allow_max_smem(topk_stream_kernel<1024, LocalSource>, smem)) != cudaSuccess) return e;
     d.configured = true;
   }
   *out = &d;
@@ -234,21 +296,28 @@ static cudaError_t device_info(DeviceInfo** out) {
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Streaming path when the row fits it (n <= 8192, K <= 2048, 16-byte copies
-// possible); the general path otherwise.
+// possible): one 1024-thread CTA per row when the rows fit on the SMs at
+// once, else two 512-thread CTAs per SM walking the rows.  The general path
+// otherwise.
 template <class Source>
-static dcp_status launch_rows(const Source& src, int T, int n, int staged_words, int K,
-                              float* out_scores, int32_t* out_ids, cudaStream_t stream) {
+static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out_scores,
+                              int32_t* out_ids, cudaStream_t stream) {
   DeviceInfo* d = nullptr;
   if (device_info(&d) != cudaSuccess) return DCP_ERR_CUDA;
-  const int grid = T < d->sms ? T : d->sms;
-  const size_t fast_smem = fast_smem_bytes(staged_words);
-  if (src.vec4 && n <= kFastMaxN && K <= kFastMaxK && fast_smem <= (size_t)d->max_smem_optin) {
-    topk_fast_kernel<Source><<<grid, kThreads, fast_smem, stream>>>(src, T, K, out_scores,
-                                                                     out_ids);
+  const int words = src.staged_words();
+  const size_t smem = stream_smem_bytes(words);
+  if (src.vec4 && n <= kStreamMaxN && K <= kStreamMaxK && smem <= (size_t)d->max_smem_optin) {
+    if (T <= d->sms) {
+      topk_stream_kernel<1024, Source><<<T, 1024, smem, stream>>>(src, T, K, out_scores, out_ids);
+    } else {
+      const int grid = T < 2 * d->sms ? T : 2 * d->sms;
+      topk_stream_kernel<512, Source><<<grid, 512, smem, stream>>>(src, T, K, out_scores, out_ids);
+    }
   } else {
-    const size_t smem = row_smem_bytes(n, K);
-    if (smem > (size_t)d->max_smem_optin) return DCP_ERR_UNSUPPORTED;
-    topk_rows_kernel<Source><<<grid, kThreads, smem, stream>>>(src, T, K, out_scores, out_ids);
+    const size_t gsmem = row_smem_bytes(n, K);
+    if (gsmem > (size_t)d->max_smem_optin) return DCP_ERR_UNSUPPORTED;
+    const int grid = T < d->sms ? T : d->sms;
+    topk_rows_kernel<Source><<<grid, kThreads, gsmem, stream>>>(src, T, K, out_scores, out_ids);
   }
   return cudaGetLastError() == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
 }
@@ -275,8 +344,7 @@ dcp_status dcp_topk_merge(const float* scores, const int32_t* ids, int T, int dc
   if (!scores || !ids || !out_ids || !out_scores) return DCP_ERR_INVALID;
   dcp::MergeSource src{scores, ids, row_starts, T, dcp_, K,
                        (K % 4) == 0 && dcp::aligned16(scores) && dcp::aligned16(ids)};
-  return dcp::launch_rows(src, T, dcp_ * K, 2 * dcp_ * K, K, out_scores, out_ids,
-                          (cudaStream_t)stream);
+  return dcp::launch_rows(src, T, dcp_ * K, K, out_scores, out_ids, (cudaStream_t)stream);
 }
 
 dcp_status dcp_local_topk(const float* logits, int T, int L, int ld, int K, int rank, int dcp_,
@@ -289,7 +357,7 @@ dcp_status dcp_local_topk(const float* logits, int T, int L, int ld, int K, int 
   if (!logits || !out_scores || !out_ids) return DCP_ERR_INVALID;
   dcp::LocalSource src{logits, row_starts, L, ld, rank,
                        (L % 4) == 0 && (ld % 4) == 0 && dcp::aligned16(logits)};
-  return dcp::launch_rows(src, T, L, L, K, out_scores, out_ids, (cudaStream_t)stream);
+  return dcp::launch_rows(src, T, L, K, out_scores, out_ids, (cudaStream_t)stream);
 }
 
 const char* dcp_status_string(dcp_status status) {

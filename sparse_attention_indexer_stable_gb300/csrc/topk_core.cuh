@@ -1,7 +1,7 @@
-// topk_core.cuh -- per-row stable top-K selection on sm_103a.
+// topk_core.cuh -- general per-row stable top-K selection on sm_103a.
 //
-// One CTA owns one query row at a time: the row's candidates sit in shared
-// memory as (32-bit score key, inverted id) pairs, and the CTA
+// One CTA of NT threads owns one query row at a time.  Given accessors for
+// each candidate's 32-bit score key and inverted id, it
 //   1. radix-selects the K-th largest score key with 11/11/10-bit digit
 //      histograms ("[Kernel] Optimize CuTeDSL DCP top-k merge", Summary: a
 //      radix pass over 32-bit score keys first),
@@ -10,8 +10,9 @@
 //      (same page: the token-id tie-break pass runs only when the score
 //      threshold actually ties),
 //   3. compacts the K winners as 64-bit keys score_key<<32 | ~id,
-//   4. sorts them descending (score descending, then lowest id),
-//   5. writes scores (bit-exact, recovered from the key) and ids.
+//   4. sorts them descending (score descending, then lowest id).
+// This is the path for rows the streaming kernel (topk_fast.cuh) does not
+// take, and its fallback for rows whose keys cluster too tightly.
 //
 // Barrier discipline: every phase that reads a shared result (threshold digit,
 // counts) is separated by __syncthreads() from the next phase that resets or
@@ -25,7 +26,7 @@
 namespace dcp {
 
 constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
+constexpr int kMaxWarps = 32;
 constexpr int kHistBins = 2048;
 
 // Order-preserving map of fp32 bits to u32: unsigned order of the result is
@@ -41,8 +42,8 @@ __device__ __forceinline__ uint32_t score_bits(uint32_t key) {
 
 struct SelectShared {
   uint32_t hist[kHistBins];
-  uint32_t warp_sum[kWarps];
-  uint32_t warp_off[kWarps];
+  uint32_t warp_sum[kMaxWarps];
+  uint32_t warp_off[kMaxWarps];
   uint32_t found_digit;
   uint32_t found_above;
   uint32_t found_count;
@@ -61,34 +62,39 @@ __device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v) {
 }
 
 // Finds the digit d of the histogram with above(d) < need <= above(d) + hist[d],
-// above(d) = sum of hist[e] for e > d.  nbins <= 2 * kThreads.  Exactly one
-// thread writes found_*; the caller must __syncthreads() before reading them.
+// above(d) = sum of hist[e] for e > d; nbins <= 2048.  Exactly one thread
+// writes found_*; the caller must __syncthreads() before reading them.
+template <int NT>
 __device__ __forceinline__ void find_threshold_digit(SelectShared& s, int nbins, uint32_t need) {
+  constexpr int kPer = kHistBins / NT;  // bins per thread, descending
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const int b0 = nbins - 1 - 2 * tid;
-  const int b1 = b0 - 1;
-  const uint32_t h0 = b0 >= 0 ? s.hist[b0] : 0u;
-  const uint32_t h1 = b1 >= 0 ? s.hist[b1] : 0u;
-  const uint32_t local = h0 + h1;
+  uint32_t h[kPer];
+  uint32_t local = 0u;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const int b = nbins - 1 - (kPer * tid + e);
+    h[e] = b >= 0 ? s.hist[b] : 0u;
+    local += h[e];
+  }
   const uint32_t incl = warp_inclusive_scan(local);
   if (lane == 31) s.warp_sum[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const uint32_t w = s.warp_sum[lane];
+    const uint32_t w = lane < NT / 32 ? s.warp_sum[lane] : 0u;
     const uint32_t wi = warp_inclusive_scan(w);
     s.warp_off[lane] = wi - w;
   }
   __syncthreads();
-  const uint32_t excl = s.warp_off[warp] + incl - local;
-  if (h0 != 0u && excl < need && need <= excl + h0) {
-    s.found_digit = (uint32_t)b0;
-    s.found_above = excl;
-    s.found_count = h0;
-  } else if (h1 != 0u && excl + h0 < need && need <= excl + local) {
-    s.found_digit = (uint32_t)b1;
-    s.found_above = excl + h0;
-    s.found_count = h1;
+  uint32_t above = s.warp_off[warp] + incl - local;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    if (h[e] != 0u && above < need && need <= above + h[e]) {
+      s.found_digit = (uint32_t)(nbins - 1 - (kPer * tid + e));
+      s.found_above = above;
+      s.found_count = h[e];
+    }
+    above += h[e];
   }
 }
 
@@ -106,7 +112,7 @@ struct RadixResult {
 
 // Radix select of the `need` largest values (1 <= need <= participants).
 // ValueFn(i, v) -> bool: whether candidate i participates, and its value.
-template <class ValueFn>
+template <int NT, class ValueFn>
 __device__ __forceinline__ RadixResult radix_select(SelectShared& s, int n, uint32_t need,
                                                     ValueFn value) {
   const int tid = threadIdx.x;
@@ -116,14 +122,14 @@ __device__ __forceinline__ RadixResult radix_select(SelectShared& s, int n, uint
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const int nbins = pass == 2 ? 1024 : 2048;
     const uint32_t dmask = (uint32_t)nbins - 1u;
-    for (int b = tid; b < nbins; b += kThreads) s.hist[b] = 0u;
+    for (int b = tid; b < nbins; b += NT) s.hist[b] = 0u;
     __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
+    for (int i = tid; i < n; i += NT) {
       uint32_t v;
       if (value(i, v) && (v & r.mask) == r.prefix) atomicAdd(&s.hist[(v >> shift) & dmask], 1u);
     }
     __syncthreads();
-    find_threshold_digit(s, nbins, r.need);
+    find_threshold_digit<NT>(s, nbins, r.need);
     __syncthreads();
     const uint32_t d = s.found_digit, above = s.found_above, cnt = s.found_count;
     r.need -= above;
@@ -139,11 +145,12 @@ __device__ __forceinline__ RadixResult radix_select(SelectShared& s, int n, uint
 }
 
 // Bitonic sort of n_pow2 64-bit keys in shared memory, descending.
+template <int NT>
 __device__ __forceinline__ void bitonic_sort_desc(unsigned long long* a, int n_pow2) {
   const int tid = threadIdx.x;
   for (int k = 2; k <= n_pow2; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < (n_pow2 >> 1); i += kThreads) {
+      for (int i = tid; i < (n_pow2 >> 1); i += NT) {
         const int lo = 2 * i - (i & (j - 1));
         const int hi = lo + j;
         const unsigned long long x = a[lo], y = a[hi];
@@ -162,7 +169,7 @@ __device__ __forceinline__ void bitonic_sort_desc(unsigned long long* a, int n_p
 // key(i) -> 32-bit score key, inv(i) -> inverted id.  On return
 // win[0..ksel) holds the winners sorted descending by 64-bit key.
 // n_pow2: a power of two >= ksel; win must have room for n_pow2 keys.
-template <class KeyFn, class InvFn>
+template <int NT, class KeyFn, class InvFn>
 __device__ __forceinline__ void select_sort_row(SelectShared& s, int n, int ksel,
                                                 unsigned long long* win, int n_pow2,
                                                 KeyFn key, InvFn inv) {
@@ -170,7 +177,7 @@ __device__ __forceinline__ void select_sort_row(SelectShared& s, int n, int ksel
   const int lane = tid & 31;
 
   // 1. Threshold on the 32-bit score key.
-  const RadixResult rs = radix_select(s, n, (uint32_t)ksel, [&](int i, uint32_t& v) {
+  const RadixResult rs = radix_select<NT>(s, n, (uint32_t)ksel, [&](int i, uint32_t& v) {
     v = key(i);
     return true;
   });
@@ -181,7 +188,7 @@ __device__ __forceinline__ void select_sort_row(SelectShared& s, int n, int ksel
   RadixResult rt{0u, 0u, 0u, 0u};
   if (tie) {
     const uint32_t tau = rs.prefix;
-    rt = radix_select(s, n, rs.need, [&](int i, uint32_t& v) {
+    rt = radix_select<NT>(s, n, rs.need, [&](int i, uint32_t& v) {
       v = inv(i);
       return key(i) == tau;
     });
@@ -195,7 +202,7 @@ __device__ __forceinline__ void select_sort_row(SelectShared& s, int n, int ksel
 
   // 3. Compaction of the winners (order is irrelevant: the sort below fixes
   //    it, and candidates with equal 64-bit keys are identical).
-  for (int base = 0; base < n; base += kThreads) {
+  for (int base = 0; base < n; base += NT) {
     const int i = base + tid;
     bool w = false;
     uint32_t k = 0u, u = 0u;
@@ -224,11 +231,11 @@ __device__ __forceinline__ void select_sort_row(SelectShared& s, int n, int ksel
       if (slot < (uint32_t)n_pow2) win[slot] = ((unsigned long long)k << 32) | u;
     }
   }
-  for (int j = ksel + tid; j < n_pow2; j += kThreads) win[j] = 0ull;
+  for (int j = ksel + tid; j < n_pow2; j += NT) win[j] = 0ull;
   __syncthreads();
 
   // 4. Final order.
-  bitonic_sort_desc(win, n_pow2);
+  bitonic_sort_desc<NT>(win, n_pow2);
 }
 
 }  // namespace dcp

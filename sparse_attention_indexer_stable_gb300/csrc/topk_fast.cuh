@@ -2,36 +2,39 @@
 // and K <= 2048 (the merge at DCP=4, K=2048 and the local top-K over 4096
 // columns fall here).
 //
-// A persistent grid of one 1024-thread CTA per SM walks the rows; each CTA
-// double-buffers its rows in shared memory with 16-byte cp.async copies, so
-// the next row streams in from HBM while the current one is selected.  The
-// selection and the final ordering come out of one two-level bucket pass
-// instead of a radix select followed by a sort:
+// A persistent grid walks the rows: CTAs of 512 threads, two per SM, for many
+// rows (one CTA's row streams in from HBM while the other CTA selects), or one
+// 1024-thread CTA per row for a few rows.  A row is staged in shared memory
+// with 16-byte cp.async copies read straight from the rank-major layout, and
+// selection and final order come out of one two-level bucket pass instead of
+// a radix select followed by a sort:
 //
-//  L1  an 11-bit histogram of the score key's top bits over every candidate
-//      (the "radix pass over 32-bit score keys first" of "[Kernel] Optimize
-//      CuTeDSL DCP top-k merge", Summary) locates the bin b1 that holds the
-//      K-th largest key; every candidate above b1 is a winner.
-//  L2  bins >= b1 are split into fine buckets, about one bucket per two
-//      candidates, on the next bits of the candidate's 64-bit key
-//      score_key<<32 | ~id below the bin prefix, skipping bits constant over
-//      the row; the token id therefore only enters when scores tie, which is
-//      the page's conditional tie-break.  Fine buckets are ordered like the
-//      keys, so a prefix sum over their counts gives each bucket its first
-//      output position.
-//  RANK each candidate in a bucket that starts before K counts the bucket
-//      members with a larger key; bucket start + that count is its output
-//      position, and positions >= K are the losers.  Buckets are small (a few
-//      members), so this is both the selection of the threshold and the sort.
+//  L1      an 11-bit histogram of the score keys' top bits over every
+//          candidate (the "radix pass over 32-bit score keys first" of
+//          "[Kernel] Optimize CuTeDSL DCP top-k merge", Summary) locates the
+//          bin b1 holding the K-th largest key; bins above b1 are all winners.
+//  COMPACT the candidates of bins >= b1 ("live", about K of them) are packed
+//          into a dense list of 64-bit keys score_key<<32 | ~id.
+//  L2      each live bin is split into fine buckets, about one per two
+//          members, on the next bits of its 64-bit key, skipping bits that
+//          are equal for all live candidates; the token id enters only where
+//          scores tie, which is the page's conditional tie-break.  Buckets are
+//          numbered in key order, so a prefix sum over their sizes gives each
+//          bucket its first output position.
+//  RANK    a live candidate in a bucket that starts before K counts the bucket
+//          members with larger keys: its output position is the bucket start
+//          plus that count, and positions >= K are the losers.  Buckets hold a
+//          few members, so this one step both finishes the selection at the
+//          threshold and sorts the winners.
 //
-// Rows whose buckets come out too large to rank this way (pathological key
-// clusters) take the radix-select + sort path of topk_core.cuh on the same
-// staged row, so results never depend on the data's distribution, only the
+// Rows whose live set or buckets come out too large for this (pathologically
+// clustered keys) take the radix-select + sort of topk_core.cuh on the same
+// staged row: the result never depends on the data's distribution, only the
 // speed does.
 //
-// Barriers: every shared array is reset only after the barrier that follows
-// its last reader in the row (the race the first page's review reports came
-// from resetting shared state that late warps had not yet read).
+// Barriers: shared state is reset only after the barrier that follows its last
+// reader in the row (the race the first page's review reports came from
+// resetting shared state that late warps had not yet read).
 #pragma once
 
 #include <cstdint>
@@ -40,34 +43,33 @@
 
 namespace dcp {
 
-constexpr int kFastItems = 8;
-constexpr int kFastMaxN = kThreads * kFastItems;  // 8192 candidates per row
-constexpr int kFastMaxK = 2048;
-constexpr int kFineMax = kFastMaxK + 1024;        // fine buckets per row, upper bound
-constexpr int kArrSlack = 256;                    // room for the bucket straddling K
-constexpr int kArrMax = kFastMaxK + kArrSlack;
-constexpr uint32_t kRankLimit = 1u << 19;         // sum of squared bucket sizes
-constexpr uint32_t kNoBucket = 0xFFFFFFFFu;
+constexpr int kStreamMaxN = 8192;             // candidates per row
+constexpr int kStreamMaxK = 2048;
+constexpr int kLiveMax = 3072;                // live candidates per row
+constexpr int kFineMax = kStreamMaxK + 1024;  // fine buckets per row (bound, see SCAN1)
+constexpr int kArrSlack = 256;                // room past K for the bucket straddling K
+constexpr uint32_t kBigBucket = 64;           // larger buckets send the row to the fallback
+constexpr uint32_t kNone = 0xFFFFFFFFu;
 
-struct FastShared {
-  SelectShared sel;                 // radix-select state of the fallback path
-  uint32_t table[kHistBins];        // L1 counts, then per bin (first bucket << 8 | log2 buckets)
-  uint32_t fcnt[kFineMax];          // L2 counts (+ 1<<16 per member of an exact bucket), then cursors
-  uint32_t fst[kFineMax];           // bucket start | count << 15 | exact << 31
-  unsigned long long arr[kArrMax];  // candidates in bucket order (fallback: sorted winners)
-  uint32_t out_s[kFastMaxK];        // winners' score bits in output order
-  int32_t out_i[kFastMaxK];         // winners' output ids
-  uint32_t wa[kWarps];
-  uint32_t wb[kWarps];
-  // OR / AND over the candidates of each key class (0: positive scores,
-  // 1: negative finite scores, 2: -inf and below) of the low 21 key bits
-  // (entries 0..2) and of the inverted ids (entries 3..5)
-  uint32_t acc_or[6];
-  uint32_t acc_and[6];
-  uint32_t b1;                      // bin of the K-th largest key
-  uint32_t nfine;                   // buckets in bins >= b1
-  uint32_t rank_work;               // sum of squared sizes of the buckets to rank
-  uint32_t arr_overflow;            // a bucket straddling K would not fit arr
+struct StreamShared {
+  unsigned long long live[kLiveMax];  // live keys; then in bucket order; fallback: sorted winners
+  uint32_t fine[kFineMax];            // L2 sizes, then start << 16 | fill cursor
+  union {
+    uint32_t table[kHistBins];        // L1 counts, then first bucket << 8 | log2(buckets)
+    SelectShared sel;                 // the fallback's radix-select state
+  } u;
+  uint32_t wa[kMaxWarps];
+  uint32_t wb[kMaxWarps];
+  uint32_t stat_or[2];                // over live finite candidates: low 21 score bits, ~id
+  uint32_t stat_and[2];
+  uint32_t live_cursor;
+  uint32_t b1;                        // L1 bin of the K-th largest key
+  uint32_t nlive;                     // candidates in bins >= b1
+  uint32_t nfine;                     // fine buckets of bins >= b1
+  uint32_t above_b1;                  // candidates in bins above b1
+  uint32_t found_digit, found_above, found_count;  // refinement of b1
+  uint32_t p_end;                     // end of the bucket straddling K
+  uint32_t overflow;                  // a bucket to rank is too large, or does not fit the list
 };
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
@@ -81,334 +83,443 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(gmem), "r"(bytes) : "memory");
+}
 
-// Buckets given to an L1 bin holding h candidates: half of h rounded up to a
-// power of two, at least 1 and at most 1024; 0 for an empty bin.
+// Fine buckets for an L1 bin of h candidates: half of h rounded up to a power
+// of two, at least 1 and at most 1024 (0 for an empty bin).  Never more than
+// h, so the bins above b1 (fewer than K candidates) get fewer than K buckets.
 __device__ __forceinline__ uint32_t fine_buckets(uint32_t h) {
-  if (h == 0u) return 0u;
-  if (h <= 2u) return 1u;
-  const uint32_t p = 1u << (32 - __clz(h - 1u));  // next power of two >= h
-  return min(p >> 1, 1024u);
+  const uint32_t p = (1u << (32 - __clz(h - 1u))) >> 1;  // next power of two >= h, halved
+  return h == 0u ? 0u : min(max(p, 1u), 1024u);
 }
 
-// Key class of a score key: 0 for positive scores, 1 for negative finite
-// scores, 2 for -inf and below (L1 bins 0..3), where padding lives.
-__device__ __forceinline__ int key_class(uint32_t k) {
-  return (k & 0x80000000u) ? 0 : ((k >> 21) <= 3u ? 2 : 1);
+// Loads P consecutive histogram words at p (ascending bins) into h in
+// descending bin order.
+template <int P>
+__device__ __forceinline__ void load_bins_desc(const uint32_t* p, uint32_t (&h)[P]) {
+  if constexpr (P == 4) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    h[0] = w.w;
+    h[1] = w.z;
+    h[2] = w.y;
+    h[3] = w.x;
+  } else if constexpr (P == 2) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    h[0] = w.y;
+    h[1] = w.x;
+  } else {
+#pragma unroll
+    for (int e = 0; e < P; ++e) h[e] = p[P - 1 - e];
+  }
 }
 
-template <class Source>
-__global__ void __launch_bounds__(kThreads, 1)
-    topk_fast_kernel(Source src, int T, int K, float* __restrict__ out_scores,
-                     int32_t* __restrict__ out_ids) {
+// Digit d of a 2048-bin histogram with above(d) < need <= above(d) + hist[d]
+// (above(d): total of the bins above d).  wa/wb: per-warp scratch.  One
+// thread writes the results; the caller synchronises before reading them.
+template <int NT>
+__device__ __forceinline__ void find_digit_desc(const uint32_t* hist, uint32_t need, uint32_t* wa,
+                                                uint32_t* wb, uint32_t& digit, uint32_t& above_out,
+                                                uint32_t& count_out) {
+  constexpr int kPer = kHistBins / NT;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t h[kPer];
+  load_bins_desc<kPer>(hist + kHistBins - kPer * (tid + 1), h);
+  uint32_t local = 0u;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) local += h[e];
+  const uint32_t incl = warp_inclusive_scan(local);
+  if (lane == 31) wa[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = lane < NT / 32 ? wa[lane] : 0u;
+    wb[lane] = warp_inclusive_scan(w) - w;
+  }
+  __syncthreads();
+  uint32_t above = wb[warp] + incl - local;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    if (h[e] != 0u && above < need && need <= above + h[e]) {
+      digit = (uint32_t)(kHistBins - 1 - (kPer * tid + e));
+      above_out = above;
+      count_out = h[e];
+    }
+    above += h[e];
+  }
+}
+
+// Shared-memory bytes of the streaming kernel for a row staging `words` words.
+inline size_t stream_smem_bytes(int words) {
+  return ((sizeof(StreamShared) + 15) & ~(size_t)15) + (size_t)((words + 3) & ~3) * 4;
+}
+
+// Zeroes `words` (a multiple of 4) 16-byte-aligned shared words.
+template <int NT>
+__device__ __forceinline__ void zero_words(uint32_t* p, int words) {
+  for (int i = 4 * (int)threadIdx.x; i < words; i += 4 * NT)
+    *reinterpret_cast<uint4*>(p + i) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+template <int NT, class Source>
+__global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
+    topk_stream_kernel(Source src, int T, int K, float* __restrict__ out_scores,
+                       int32_t* __restrict__ out_ids) {
+  constexpr int kWarpsT = NT / 32;
+  constexpr int kVec = kStreamMaxN / 4 / NT;  // 16-byte score chunks per thread
+  constexpr int kItems = 4 * kVec;
+  constexpr int kLivePer = kLiveMax / NT;
+  constexpr int kFinePer = kFineMax / NT;
+  constexpr int kBinsPer = kHistBins / NT;
+
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  FastShared& s = *reinterpret_cast<FastShared*>(smem_raw);
-  const int n = src.count();
-  const int words = (src.staged_words() + 3) & ~3;
-  uint32_t* rowbuf = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(FastShared) + 15) & ~(size_t)15));
+  StreamShared& s = *reinterpret_cast<StreamShared*>(smem_raw);
+  uint32_t* stage =
+      reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(StreamShared) + 15) & ~(size_t)15));
+  const int n = src.count();  // multiple of 4, <= kStreamMaxN
+  const int n4 = n >> 2;
   const int ksel = K < n ? K : n;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
 
-  for (int i = tid; i < kHistBins; i += kThreads) s.table[i] = 0u;
-  for (int i = tid; i < kFineMax; i += kThreads) s.fcnt[i] = 0u;
-  if (tid < 6) {
-    s.acc_or[tid] = 0u;
-    s.acc_and[tid] = 0xFFFFFFFFu;
-  }
+  zero_words<NT>(s.u.table, kHistBins);
+  zero_words<NT>(s.fine, kFineMax);
   if (tid == 0) {
-    s.rank_work = 0u;
-    s.arr_overflow = 0u;
+    s.live_cursor = 0u;
+    s.overflow = 0u;
+    s.stat_or[0] = s.stat_or[1] = 0u;
+    s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
   }
 
-  // Rows of this CTA: t = blockIdx.x + k * gridDim.x.  Walking the 1024-row
-  // chunks in order and taking the rows congruent to blockIdx.x in each
-  // visits exactly this sequence, so the walk is chunk by chunk.
+  // This CTA's rows are t = blockIdx.x + k * gridDim.x: walking the rows in
+  // chunks of 1024 and taking, in each, the rows congruent to blockIdx.x
+  // visits exactly this sequence.
   const int G = (int)gridDim.x;
   int t = (int)blockIdx.x;
-  if (t < T) src.issue(t, rowbuf);
+  if (t < T) src.template issue<NT>(t, stage);
   cp_async_commit();
-  if (t + G < T) src.issue(t + G, rowbuf + words);
-  cp_async_commit();
+  if (tid == 0 && t + G < T) src.prefetch_l2(t + G);
 
-  for (int k = 0; t < T; ++k, t += G) {
-    uint32_t* cur = rowbuf + (k & 1) * words;
-    cp_async_wait<1>();
-    __syncthreads();  // this row is staged; the previous row's state is reset
+  for (; t < T; t += G) {
+    cp_async_wait<0>();
+    __syncthreads();  // the row is staged and the previous row's state reset
+    // Rows stream from HBM into L2 two rows ahead of their use; the copy of
+    // the next row into shared memory starts as soon as this row's staged
+    // data is consumed (after COMPACT).
+    if (tid == 0 && t + 2 * G < T) src.prefetch_l2(t + 2 * G);
 
-    // ---- L1: top-11-bit histogram; constant-bit masks per key class -----
-    uint32_t keys[kFastItems], invs[kFastItems], slot[kFastItems];
-    uint32_t lor[3] = {0u, 0u, 0u}, land[3] = {~0u, ~0u, ~0u};
-    uint32_t ior[3] = {0u, 0u, 0u}, iand[3] = {~0u, ~0u, ~0u};
+    // ---- L1: histogram of the score keys' top 11 bits ---------------------
+    uint32_t keys[kItems];
 #pragma unroll
-    for (int j = 0; j < kFastItems; ++j) {
-      const int i = tid + j * kThreads;
-      keys[j] = 0u;
-      invs[j] = 0u;
-      if (i < n) {
-        const uint32_t kk = score_key(cur[i]);
-        const uint32_t u = src.inv(cur, i);
-        keys[j] = kk;
-        invs[j] = u;
-        atomicAdd(&s.table[kk >> 21], 1u);
-        const uint32_t lo = kk & 0x1FFFFFu;
-        const int c = key_class(kk);
+    for (int v = 0; v < kVec; ++v) {
+      const int c = tid + v * NT;
+      if (c < n4) {
+        const uint4 w = *reinterpret_cast<const uint4*>(stage + 4 * c);
+        keys[4 * v + 0] = score_key(w.x);
+        keys[4 * v + 1] = score_key(w.y);
+        keys[4 * v + 2] = score_key(w.z);
+        keys[4 * v + 3] = score_key(w.w);
 #pragma unroll
-        for (int e = 0; e < 3; ++e) {
-          if (c == e) {
-            lor[e] |= lo;
-            land[e] &= lo;
-            ior[e] |= u;
-            iand[e] &= u;
+        for (int e = 0; e < 4; ++e) atomicAdd(&s.u.table[keys[4 * v + e] >> 21], 1u);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) keys[4 * v + e] = 0u;
+      }
+    }
+    __syncthreads();
+
+    // ---- SCAN1: bins high to low; packed (buckets << 16 | candidates) -------
+    {
+      uint32_t h[kBinsPer], f[kBinsPer];
+      load_bins_desc<kBinsPer>(s.u.table + kHistBins - kBinsPer * (tid + 1), h);
+      uint32_t local = 0u;
+#pragma unroll
+      for (int e = 0; e < kBinsPer; ++e) {
+        f[e] = fine_buckets(h[e]);
+        local += (f[e] << 16) | h[e];
+      }
+      const uint32_t incl = warp_inclusive_scan(local);
+      if (lane == 31) s.wa[warp] = incl;
+      __syncthreads();
+      // every warp scans the per-warp totals itself (no second barrier)
+      const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
+      const uint32_t wti = warp_inclusive_scan(wt);
+      uint32_t ex = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
+#pragma unroll
+      for (int e = 0; e < kBinsPer; ++e) {
+        const uint32_t above = ex & 0xFFFFu, fabove = ex >> 16;
+        const int b = kHistBins - 1 - (kBinsPer * tid + e);
+        if (h[e] != 0u) {
+          if (above < (uint32_t)ksel && (uint32_t)ksel <= above + h[e]) {
+            s.b1 = (uint32_t)b;
+            s.nlive = above + h[e];
+            s.nfine = fabove + f[e];
+            s.above_b1 = above;
+          }
+          s.u.table[b] = (fabove << 8) | (uint32_t)(31 - __clz(f[e]));
+        }
+        ex += (f[e] << 16) | h[e];
+      }
+    }
+    __syncthreads();
+
+    const uint32_t b1 = s.b1;
+    const int nfine = (int)s.nfine;
+    // Live candidates are those with (key >> 10) >= live_from.  Normally that
+    // is every candidate of bins >= b1; when bin b1 alone is too full for the
+    // live list, its next 11 key bits are histogrammed (in `fine`, still
+    // zero) and only its candidates from the digit holding the K-th key on
+    // are kept live.
+    uint32_t live_from = b1 << 11;
+    if (s.nlive > (uint32_t)kLiveMax) {
+#pragma unroll
+      for (int j = 0; j < kItems; ++j) {
+        if ((tid + (j >> 2) * NT) < n4 && (keys[j] >> 21) == b1)
+          atomicAdd(&s.fine[(keys[j] >> 10) & 0x7FFu], 1u);
+      }
+      __syncthreads();
+      find_digit_desc<NT>(s.fine, (uint32_t)ksel - s.above_b1, s.wa, s.wb, s.found_digit,
+                          s.found_above, s.found_count);
+      __syncthreads();
+      live_from |= s.found_digit;
+      const uint32_t nl = s.above_b1 + s.found_above + s.found_count;
+      zero_words<NT>(s.fine, kHistBins);
+      __syncthreads();
+      if (tid == 0) s.nlive = nl;
+      __syncthreads();
+    }
+    const int nlive = (int)s.nlive;
+    bool fast = nlive <= kLiveMax;
+
+    // ---- COMPACT: live candidates into a dense list -------------------------
+    if (fast) {
+      uint32_t mask = 0u, cnt = 0u;
+#pragma unroll
+      for (int j = 0; j < kItems; ++j) {
+        const bool lv = (tid + (j >> 2) * NT) < n4 && (keys[j] >> 10) >= live_from;
+        mask |= (lv ? 1u : 0u) << j;
+        cnt += lv ? 1u : 0u;
+      }
+      const uint32_t incl = warp_inclusive_scan(cnt);
+      uint32_t base = 0u;
+      if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
+      unsigned long long* dst = s.live + (__shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt);
+#pragma unroll
+      for (int v = 0; v < kVec; ++v) {
+        if ((mask >> (4 * v)) & 0xFu) {
+          const uint4 u4 = src.inv4(stage, tid + v * NT);
+          const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (mask & (1u << (4 * v + e)))
+              *dst++ = ((unsigned long long)keys[4 * v + e] << 32) | us[e];
           }
         }
       }
     }
+    __syncthreads();
+    // The staged row is consumed (the fallback re-reads its row from global
+    // memory): stream the next row in behind the rest of this one.
+    if (t + G < T) src.template issue<NT>(t + G, stage);
+    cp_async_commit();
+
+    // ---- L2: live keys into registers; which bits vary over them ----------
+    unsigned long long lkey[kLivePer];
+    uint32_t gslot[kLivePer];
+    if (fast) {
+      uint32_t lor = 0u, land = 0xFFFFFFFFu, ior = 0u, iand = 0xFFFFFFFFu;
 #pragma unroll
-    for (int e = 0; e < 3; ++e) {
-      lor[e] = __reduce_or_sync(0xFFFFFFFFu, lor[e]);
-      land[e] = __reduce_and_sync(0xFFFFFFFFu, land[e]);
-      ior[e] = __reduce_or_sync(0xFFFFFFFFu, ior[e]);
-      iand[e] = __reduce_and_sync(0xFFFFFFFFu, iand[e]);
-    }
-    if (lane < 3) {
-      // lane e publishes class e (all lanes hold the reduced values)
-#pragma unroll
-      for (int e = 0; e < 3; ++e) {
-        if (lane == e) {
-          atomicOr(&s.acc_or[e], lor[e]);
-          atomicAnd(&s.acc_and[e], land[e]);
-          atomicOr(&s.acc_or[3 + e], ior[e]);
-          atomicAnd(&s.acc_and[3 + e], iand[e]);
+      for (int u = 0; u < kLivePer; ++u) {
+        const int e = tid + u * NT;
+        lkey[u] = e < nlive ? s.live[e] : 0ull;
+        const uint32_t k = (uint32_t)(lkey[u] >> 32);
+        if (e < nlive && (k >> 21) > 3u) {  // finite score
+          const uint32_t lo = ((k & 0x80000000u) ? k : ~k) & 0x1FFFFFu;
+          lor |= lo;
+          land &= lo;
+          ior |= (uint32_t)lkey[u];
+          iand &= (uint32_t)lkey[u];
         }
       }
+      lor = __reduce_or_sync(0xFFFFFFFFu, lor);
+      land = __reduce_and_sync(0xFFFFFFFFu, land);
+      ior = __reduce_or_sync(0xFFFFFFFFu, ior);
+      iand = __reduce_and_sync(0xFFFFFFFFu, iand);
+      if (lane == 0) {
+        atomicOr(&s.stat_or[0], lor);
+        atomicAnd(&s.stat_and[0], land);
+        atomicOr(&s.stat_or[1], ior);
+        atomicAnd(&s.stat_and[1], iand);
+      }
     }
     __syncthreads();
 
-    // ---- SCAN1: bins in descending order; (buckets << 16 | count) packed --
-    {
-      const int bA = kHistBins - 1 - 2 * tid;
-      const int bB = bA - 1;
-      const uint32_t hA = s.table[bA], hB = s.table[bB];
-      const uint32_t fA = fine_buckets(hA), fB = fine_buckets(hB);
-      const uint32_t v = ((fA + fB) << 16) | (hA + hB);
-      const uint32_t incl = warp_inclusive_scan(v);
-      if (lane == 31) s.wa[warp] = incl;
-      __syncthreads();
-      if (warp == 0) {
-        const uint32_t w = s.wa[lane];
-        s.wb[lane] = warp_inclusive_scan(w) - w;
-      }
-      __syncthreads();
-      const uint32_t ex = s.wb[warp] + incl - v;
-      const uint32_t cA = ex & 0xFFFFu, gA = ex >> 16;
-      const uint32_t cB = cA + hA, gB = gA + fA;
-      const uint32_t need = (uint32_t)ksel;
-      if (hA != 0u && cA < need && need <= cA + hA) {
-        s.b1 = (uint32_t)bA;
-        s.nfine = gA + fA;
-      } else if (hB != 0u && cB < need && need <= cB + hB) {
-        s.b1 = (uint32_t)bB;
-        s.nfine = gB + fB;
-      }
-      if (hA != 0u) s.table[bA] = (gA << 8) | (uint32_t)(31 - __clz(fA));
-      if (hB != 0u) s.table[bB] = (gB << 8) | (uint32_t)(31 - __clz(fB));
-    }
-    __syncthreads();
-
-    // ---- L2: fine buckets for bins >= b1 ---------------------------------
-    {
-      const uint32_t b1 = s.b1;
-      // Within key class c, the low 21 key bits below tz[c] are the same for
-      // every candidate, and so are the bits of ~id at or above ib[c]; the
-      // remaining bits, key bits first, order the candidates of one bin.
-      int tz[3], ib[3];
+    // ---- L2: fine bucket of every live candidate ---------------------------
+    if (fast) {
+      // For finite scores: the low 21 key bits below tzf, and the bits of ~id
+      // at or above ibf, are equal for every live candidate, so within one bin
+      // keys are ordered like y = (low key bits >> tzf) << ibf | (~id low ibf
+      // bits), a wf-bit number whose top q bits name the bucket.  Bins 0..3
+      // (-inf, where padding lives, and below) keep every bit (53).
+      const uint32_t vk = s.stat_or[0] ^ s.stat_and[0];
+      const uint32_t vi = s.stat_or[1] ^ s.stat_and[1];
+      const int tzf = vk ? min(__ffs(vk) - 1, 21) : 21;
+      const int ibf = vi ? 32 - __clz(vi) : 0;
+      const uint32_t imask = ibf >= 32 ? 0xFFFFFFFFu : ((1u << ibf) - 1u);
+      const int wf = 21 - tzf + ibf;
 #pragma unroll
-      for (int e = 0; e < 3; ++e) {
-        const uint32_t vk = s.acc_or[e] ^ s.acc_and[e];
-        const uint32_t vi = s.acc_or[3 + e] ^ s.acc_and[3 + e];
-        tz[e] = vk ? min(__ffs(vk) - 1, 21) : 21;
-        ib[e] = vi ? 32 - __clz(vi) : 0;
-      }
-#pragma unroll
-      for (int j = 0; j < kFastItems; ++j) {
-        const int i = tid + j * kThreads;
-        slot[j] = kNoBucket;
-        if (i < n && (keys[j] >> 21) >= b1) {
-          const uint32_t tb = s.table[keys[j] >> 21];
+      for (int u = 0; u < kLivePer; ++u) {
+        gslot[u] = kNone;
+        if (tid + u * NT < nlive) {
+          const uint32_t k = (uint32_t)(lkey[u] >> 32);
+          const uint32_t inv = (uint32_t)lkey[u];
+          const uint32_t bin = k >> 21;
+          const uint32_t tb = s.u.table[bin];
           const int q = (int)(tb & 0xFFu);
-          const int c = key_class(keys[j]);
-          const int tzc = c == 0 ? tz[0] : (c == 1 ? tz[1] : tz[2]);
-          const int ibc = c == 0 ? ib[0] : (c == 1 ? ib[1] : ib[2]);
-          const uint32_t imask = ibc >= 32 ? 0xFFFFFFFFu : ((1u << ibc) - 1u);
-          const int w = (21 - tzc) + ibc;
-          const unsigned long long r =
-              ((unsigned long long)((keys[j] & 0x1FFFFFu) >> tzc) << ibc) | (invs[j] & imask);
-          const uint32_t sub = w >= q ? (uint32_t)(r >> (w - q)) : (uint32_t)(r << (q - w));
+          unsigned long long y;
+          int w;
+          if (bin > 3u) {
+            y = ((unsigned long long)((k & 0x1FFFFFu) >> tzf) << ibf) | (inv & imask);
+            w = wf;
+          } else {
+            y = ((unsigned long long)(k & 0x1FFFFFu) << 32) | inv;
+            w = 53;
+          }
+          const uint32_t sub = w >= q ? (uint32_t)(y >> (w - q)) : (uint32_t)(y << (q - w));
           const uint32_t g = (tb >> 8) + ((1u << q) - 1u - sub);
-          atomicAdd(&s.fcnt[g], w <= q ? 0x10001u : 1u);
-          slot[j] = g;
+          atomicAdd(&s.fine[g], 1u);
+          gslot[u] = g;
         }
       }
     }
     __syncthreads();
 
-    // ---- SCAN2: bucket starts; can this row be ranked in place? ----------
-    {
-      const uint32_t nf = s.nfine;
-      uint32_t c[3], ex3[3];
-      uint32_t sum = 0u;
+    // ---- SCAN2: bucket starts ------------------------------------------------
+    if (fast) {
+      uint32_t c[kFinePer];
+      uint32_t local = 0u;
 #pragma unroll
-      for (int e = 0; e < 3; ++e) {
-        const uint32_t g = (uint32_t)(3 * tid + e);
-        const uint32_t raw = g < nf ? s.fcnt[g] : 0u;
-        c[e] = raw & 0xFFFFu;
-        ex3[e] = raw >> 16;
-        sum += c[e];
+      for (int e = 0; e < kFinePer; ++e) {
+        const int g = kFinePer * tid + e;
+        c[e] = g < nfine ? s.fine[g] : 0u;
+        local += c[e];
       }
-      const uint32_t incl = warp_inclusive_scan(sum);
+      const uint32_t incl = warp_inclusive_scan(local);
       if (lane == 31) s.wa[warp] = incl;
       __syncthreads();
-      if (warp == 0) {
-        const uint32_t w = s.wa[lane];
-        s.wb[lane] = warp_inclusive_scan(w) - w;
-      }
-      __syncthreads();
-      uint32_t st = s.wb[warp] + incl - sum;
-      uint32_t work = 0u, over = 0u;
+      const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
+      const uint32_t wti = warp_inclusive_scan(wt);
+      uint32_t st = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
+      uint32_t over = 0u;
 #pragma unroll
-      for (int e = 0; e < 3; ++e) {
-        const uint32_t g = (uint32_t)(3 * tid + e);
-        if (g < nf) {
-          const bool exact = ex3[e] != 0u;
-          s.fst[g] = st | (c[e] << 15) | (exact ? 0x80000000u : 0u);
-          s.fcnt[g] = 0u;
-          if (st < (uint32_t)ksel && !exact && c[e] > 1u) {
-            work += c[e] * c[e];
-            if (st + c[e] > (uint32_t)(ksel + kArrSlack)) over = 1u;
+      for (int e = 0; e < kFinePer; ++e) {
+        const int g = kFinePer * tid + e;
+        if (g < nfine) {
+          s.fine[g] = st << 16;
+          if (st < (uint32_t)ksel) {
+            // the list holds ksel + kArrSlack keys; ranking is quadratic
+            // in a bucket's size
+            if (st + c[e] > (uint32_t)(ksel + kArrSlack) || c[e] > kBigBucket) over = 1u;
+            if ((uint32_t)ksel <= st + c[e]) s.p_end = st + c[e];
           }
           st += c[e];
         }
       }
-      work = __reduce_add_sync(0xFFFFFFFFu, work);
       over = __reduce_or_sync(0xFFFFFFFFu, over);
-      if (lane == 0 && (work | over)) {
-        atomicAdd(&s.rank_work, work);
-        atomicOr(&s.arr_overflow, over);
-      }
-      // L1/L2 state is no longer read in this row: reset it for the next.
-      for (int i = tid; i < kHistBins; i += kThreads) s.table[i] = 0u;
-      if (tid < 6) {
-        s.acc_or[tid] = 0u;
-        s.acc_and[tid] = 0xFFFFFFFFu;
-      }
+      if (lane == 0 && over) s.overflow = 1u;
     }
     __syncthreads();
+    fast = fast && s.overflow == 0u;
 
     float* os = out_scores + (size_t)t * (size_t)K;
     int32_t* oi = out_ids + (size_t)t * (size_t)K;
-    const bool fast = s.arr_overflow == 0u && s.rank_work <= kRankLimit;
-
     if (fast) {
-      // ---- SCATTER: bucket members that can still be winners, into arr --
-      const uint32_t kcap = (uint32_t)(ksel + kArrSlack);
+      // ---- SCATTER: members of buckets starting before K, in bucket order --
+      // The L1 table is no longer read: it now holds, per list position, the
+      // bucket of the key there.
+      uint16_t* bucket_of = reinterpret_cast<uint16_t*>(s.u.table);
 #pragma unroll
-      for (int j = 0; j < kFastItems; ++j) {
-        if (slot[j] != kNoBucket) {
-          const uint32_t g = slot[j];
-          const uint32_t meta = s.fst[g];
-          const uint32_t st = meta & 0x7FFFu;
-          const bool exact = (meta >> 31) != 0u;
-          uint32_t pos = kNoBucket;
+      for (int u = 0; u < kLivePer; ++u) {
+        if (gslot[u] != kNone) {
+          const uint32_t old = atomicAdd(&s.fine[gslot[u]], 1u);
+          const uint32_t st = old >> 16;
           if (st < (uint32_t)ksel) {
-            pos = st + atomicAdd(&s.fcnt[g], 1u);
-            if (pos < (exact ? (uint32_t)ksel : kcap))
-              s.arr[pos] = ((unsigned long long)keys[j] << 32) | invs[j];
-            else
-              pos = kNoBucket;
+            const uint32_t pos = st + (old & 0xFFFFu);
+            s.live[pos] = lkey[u];
+            bucket_of[pos] = (uint16_t)gslot[u];
           }
-          slot[j] = pos == kNoBucket ? kNoBucket : (g | (pos << 16));
         }
       }
       __syncthreads();
-      // The staged row is consumed: stream the row after next into it.
-      if (t + 2 * G < T) src.issue(t + 2 * G, cur);
-      cp_async_commit();
-      for (int i = tid; i < kFineMax; i += kThreads) s.fcnt[i] = 0u;
-      if (tid == 0) {
-        s.rank_work = 0u;
-        s.arr_overflow = 0u;
-      }
 
-      // ---- RANK: position = bucket start + members with a larger key -----
+      // ---- RANK: in list order, position = bucket start + larger members ---
+      const uint32_t p_end = s.p_end;
+      const uint32_t rbase = src.row_base(t);
+      for (uint32_t p = tid; p < p_end; p += NT) {
+        const unsigned long long mine = s.live[p];
+        const uint32_t meta = s.fine[bucket_of[p]];
+        const uint32_t st = meta >> 16, cnt = meta & 0xFFFFu;
+        uint32_t fin = p;
+        if (cnt > 1u) {
+          uint32_t r = 0u;
+          if (cnt <= 4u) {
+            // the bucket lies within [p - 3, p + 3]: members before p rank
+            // above it when not smaller, members after it when larger
 #pragma unroll
-      for (int j = 0; j < kFastItems; ++j) {
-        if (slot[j] != kNoBucket) {
-          const uint32_t g = slot[j] & 0xFFFFu;
-          const uint32_t pos = slot[j] >> 16;
-          const uint32_t meta = s.fst[g];
-          const uint32_t st = meta & 0x7FFFu;
-          const uint32_t cnt = (meta >> 15) & 0x7FFFu;
-          uint32_t fin = pos;
-          if ((meta >> 31) == 0u && cnt > 1u) {
-            const unsigned long long mine = ((unsigned long long)keys[j] << 32) | invs[j];
-            uint32_t r = 0u;
-            for (uint32_t e = st; e < st + cnt; ++e) {
-              const unsigned long long o = s.arr[e];
-              r += (o > mine || (o == mine && e < pos)) ? 1u : 0u;
+            for (int d = 1; d <= 3; ++d) {
+              if (p - (uint32_t)d - st < cnt) r += s.live[p - d] >= mine ? 1u : 0u;
+              if (p + (uint32_t)d - st < cnt) r += s.live[p + d] > mine ? 1u : 0u;
             }
-            fin = st + r;
+          } else {
+            for (uint32_t e = st; e < st + cnt; ++e) {
+              const unsigned long long o = s.live[e];
+              r += (o > mine || (e < p && o == mine)) ? 1u : 0u;
+            }
           }
-          if (fin < (uint32_t)ksel) {
-            s.out_s[fin] = score_bits(keys[j]);
-            s.out_i[fin] = src.out_id(t, invs[j]);
-          }
+          fin = st + r;
+        }
+        if (fin < (uint32_t)ksel) {
+          os[fin] = __uint_as_float(score_bits((uint32_t)(mine >> 32)));
+          oi[fin] = src.out_id_from(rbase, (uint32_t)mine);
         }
       }
-      __syncthreads();
-
-      // ---- STORE ----------------------------------------------------------
-      for (int j = tid; j < K; j += kThreads) {
-        if (j < ksel) {
-          os[j] = __uint_as_float(s.out_s[j]);
-          oi[j] = s.out_i[j];
-        } else {
-          os[j] = __uint_as_float(0xFF800000u);
-          oi[j] = -1;
-        }
+      for (int j = ksel + tid; j < K; j += NT) {
+        os[j] = __uint_as_float(0xFF800000u);
+        oi[j] = -1;
       }
     } else {
-      // ---- Fallback: radix select + sort on the staged row ---------------
+      // ---- Fallback: radix select + sort on the staged row -----------------
       int n_pow2 = 1;
       while (n_pow2 < ksel) n_pow2 <<= 1;
-      select_sort_row(
-          s.sel, n, ksel, s.arr, n_pow2, [&](int i) { return score_key(cur[i]); },
-          [&](int i) { return src.inv(cur, i); });
-      for (int j = tid; j < K; j += kThreads) {
+      select_sort_row<NT>(
+          s.u.sel, n, ksel, s.live, n_pow2, [&](int i) { return src.key_global(t, i); },
+          [&](int i) { return src.inv_global(t, i); });
+      const uint32_t rbase = src.row_base(t);
+      for (int j = tid; j < K; j += NT) {
         if (j < ksel) {
-          const unsigned long long w = s.arr[j];
+          const unsigned long long w = s.live[j];
           os[j] = __uint_as_float(score_bits((uint32_t)(w >> 32)));
-          oi[j] = src.out_id(t, (uint32_t)w);
+          oi[j] = src.out_id_from(rbase, (uint32_t)w);
         } else {
           os[j] = __uint_as_float(0xFF800000u);
           oi[j] = -1;
         }
       }
-      __syncthreads();  // every read of the staged row, arr and `fast` is done
-      if (t + 2 * G < T) src.issue(t + 2 * G, cur);
-      cp_async_commit();
-      if (tid == 0) {
-        s.rank_work = 0u;
-        s.arr_overflow = 0u;
-      }
+    }
+    __syncthreads();  // every reader of this row's shared state is done
+
+    zero_words<NT>(s.u.table, kHistBins);
+    zero_words<NT>(s.fine, kFineMax);
+    if (tid == 0) {
+      s.live_cursor = 0u;
+      s.overflow = 0u;
+      s.stat_or[0] = s.stat_or[1] = 0u;
+      s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
     }
   }
   cp_async_wait<0>();
-}
-
-inline size_t fast_smem_bytes(int staged_words) {
-  const size_t words = (size_t)((staged_words + 3) & ~3);
-  return ((sizeof(FastShared) + 15) & ~(size_t)15) + 2 * words * sizeof(uint32_t);
 }
 
 }  // namespace dcp
