@@ -379,10 +379,19 @@ def decode_and_sweep(torch, dk, dev, stream):
                 dk.local_topk(logits[r], K, r, dcp, out_scores=cs[r], out_ids=ci[r], stream=stream)
             dk.merge(cs, ci, out_ids=oi, out_scores=os_, stream=stream)
 
+        fo_s = torch.empty((T, K), dtype=torch.float32, device=dev)
+        fo_i = torch.empty((T, K), dtype=torch.int32, device=dev)
+
+        def fused():
+            dk.fused_topk(logits, K, out_scores=fo_s, out_ids=fo_i, stream=stream)
+
         sweep[str(T)] = {"us_per_step_launch": median_of_reps(torch, fn, stream, launches=50),
                          "us_per_step_graph": median_of_reps(torch, fn, stream, launches=50,
-                                                             graph=True)}
-    out["sweep_local4_plus_merge"] = sweep
+                                                             graph=True),
+                         "fused_us_per_launch": median_of_reps(torch, fused, stream, launches=50),
+                         "fused_us_per_graph_replay": median_of_reps(torch, fused, stream,
+                                                                     launches=50, graph=True)}
+    out["sweep_local4_plus_merge_and_fused"] = sweep
     return out
 
 

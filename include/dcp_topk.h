@@ -124,6 +124,57 @@ dcp_status dcp_local_topk(const float* logits, int T, int L, int ld, int K, int 
                           const int32_t* row_starts, float* out_scores, int32_t* out_ids,
                           dcp_stream_t stream);
 
+/*
+ * dcp_fused_topk -- the local top-K of every shard and their merge in one
+ * pass: the global top-K over all dcp*L logits of each row.  Each rank keeps
+ * the local top-K of its shard and the merge picks the global top-K of those
+ * ("[Kernel] Optimize CuTeDSL DCP top-k merge", Summary); every global winner
+ * is among its shard's local top-K, so selecting straight from the logits
+ * gives the same result as dcp_local_topk on every shard followed by
+ * dcp_topk_merge, without the candidate round trip through memory.
+ *
+ *   logits      fp32 [dcp][T][ld], rank-major: shard r's row t starts at
+ *               logits + (r*T + t)*ld; its first L columns are candidates.
+ *   T, dcp      rows and shards.  T == 0 is a no-op returning DCP_OK.
+ *   L, ld       columns per shard and row stride in elements (ld >= L).
+ *   K           outputs per row; rows with dcp*L < K are padded (-inf, -1).
+ *   row_starts  int32 [T] or NULL (all zero).
+ *   out_scores  fp32  [T][K] row-major, sorted as for the merge.
+ *   out_ids     int32 [T][K]: global ids row_starts[t] + r*L + column.
+ *
+ * Errors: DCP_ERR_INVALID for T < 0, dcp < 1, L < 1, ld < L, K < 1, or a NULL
+ * logits/out pointer with T > 0; DCP_ERR_UNSUPPORTED for K > DCP_MAX_K or
+ * dcp*L > DCP_MAX_CANDIDATES; DCP_ERR_CUDA if the launch fails.
+ */
+dcp_status dcp_fused_topk(const float* logits, int T, int dcp, int L, int ld, int K,
+                          const int32_t* row_starts, float* out_scores, int32_t* out_ids,
+                          dcp_stream_t stream);
+
+/*
+ * dcp_topk_device_status -- reads and clears the device-side status word of
+ * the current device.  Kernels that stage rows with bulk copies wait for each
+ * copy with a bounded poll (about a second); if a copy never lands, the
+ * kernel sets DCP_DEVICE_COPY_TIMEOUT here and its CTA stops, leaving its
+ * remaining rows unwritten.  0 means no failure since the last read.
+ *
+ *   status  host pointer receiving the word (DCP_ERR_INVALID if NULL).
+ *
+ * Synchronises the device first (cudaDeviceSynchronize), so call it outside
+ * any stream capture.  DCP_ERR_CUDA on a CUDA error.  This diagnostic has no
+ * counterpart on the pages; it is how a bounded wait reports that it gave up.
+ */
+#define DCP_DEVICE_COPY_TIMEOUT 1u
+dcp_status dcp_topk_device_status(unsigned int* status);
+
+/*
+ * dcp_topk_selftest_wait_timeout -- launches, on `stream`, one CTA that arms
+ * a copy barrier for a copy it never issues and waits for it for at most
+ * `wait_cycles` SM clock cycles, so that the timeout path runs: the next
+ * dcp_topk_device_status then reports DCP_DEVICE_COPY_TIMEOUT.  For tests;
+ * no counterpart on the pages.  DCP_ERR_CUDA if the launch fails.
+ */
+dcp_status dcp_topk_selftest_wait_timeout(unsigned int wait_cycles, dcp_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* dcp_status_string(dcp_status status);
 

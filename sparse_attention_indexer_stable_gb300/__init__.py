@@ -22,12 +22,15 @@ __all__ = [
     "DCP_OK", "DCP_ERR_INVALID", "DCP_ERR_UNSUPPORTED", "DCP_ERR_CUDA",
     "DCP_MAX_K", "DCP_MAX_CANDIDATES", "DcpError",
     "dcp_topk_merge", "dcp_topk_merge_workspace_size", "dcp_local_topk", "dcp_status_string",
+    "dcp_fused_topk", "dcp_topk_device_status", "dcp_topk_selftest_wait_timeout",
+    "DCP_DEVICE_COPY_TIMEOUT", "fused_topk",
     "merge", "local_topk", "library", "library_path",
 ]
 
 DCP_OK, DCP_ERR_INVALID, DCP_ERR_UNSUPPORTED, DCP_ERR_CUDA = 0, 1, 2, 3
 DCP_MAX_K = 4096
 DCP_MAX_CANDIDATES = 16384
+DCP_DEVICE_COPY_TIMEOUT = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +64,12 @@ def library():
             lib.dcp_topk_merge_workspace_size.restype = I
             lib.dcp_local_topk.argtypes = [P, I, I, I, I, I, I, P, P, P, P]
             lib.dcp_local_topk.restype = I
+            lib.dcp_fused_topk.argtypes = [P, I, I, I, I, I, P, P, P, P]
+            lib.dcp_fused_topk.restype = I
+            lib.dcp_topk_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+            lib.dcp_topk_device_status.restype = I
+            lib.dcp_topk_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
+            lib.dcp_topk_selftest_wait_timeout.restype = I
             lib.dcp_status_string.argtypes = [I]
             lib.dcp_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -90,6 +99,25 @@ def dcp_local_topk(logits, T, L, ld, K, rank, dcp, row_starts, out_scores, out_i
                    stream=None) -> int:
     return library().dcp_local_topk(logits, T, L, ld, K, rank, dcp, row_starts, out_scores,
                                     out_ids, stream)
+
+
+def dcp_fused_topk(logits, T, dcp, L, ld, K, row_starts, out_scores, out_ids,
+                   stream=None) -> int:
+    return library().dcp_fused_topk(logits, T, dcp, L, ld, K, row_starts, out_scores, out_ids,
+                                    stream)
+
+
+def dcp_topk_device_status():
+    """Read and clear the device status word (synchronises the device)."""
+    v = ctypes.c_uint(0)
+    st = library().dcp_topk_device_status(ctypes.byref(v))
+    if st != DCP_OK:
+        raise DcpError(st, "dcp_topk_device_status")
+    return v.value
+
+
+def dcp_topk_selftest_wait_timeout(wait_cycles, stream=None) -> int:
+    return library().dcp_topk_selftest_wait_timeout(int(wait_cycles), stream)
 
 
 # ------------------------------------------------------- tensor conveniences
@@ -190,4 +218,42 @@ def local_topk(logits, K, rank, dcp, L=None, row_starts=None, out_scores=None, o
                             out_scores.data_ptr(), out_ids.data_ptr(), _stream_handle(stream))
     if st != DCP_OK:
         raise DcpError(st, "dcp_local_topk")
+    return out_scores, out_ids
+
+
+def fused_topk(logits, K, L=None, row_starts=None, out_scores=None, out_ids=None, stream=None):
+    """Top-K over all shards' logits at once (local top-K + merge in one pass).
+
+    logits: float32 (dcp, T, ld) CUDA tensor, contiguous in its last two dims;
+    the first L columns of each row are candidates.  Returns
+    (out_scores float32 (T, K), out_ids int32 (T, K)).
+    """
+    torch = _torch()
+    if not isinstance(logits, torch.Tensor) or logits.dtype != torch.float32 or not logits.is_cuda:
+        raise TypeError("logits must be a float32 CUDA tensor")
+    if logits.dim() != 3 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous (dcp, T, ld) tensor")
+    dev = logits.device
+    dcp, T, ld = logits.shape
+    L = ld if L is None else int(L)
+    if L > ld:
+        raise ValueError("L exceeds the logits' columns")
+    if row_starts is not None:
+        _check(row_starts, "row_starts", torch.int32, dev)
+        if row_starts.shape != (T,):
+            raise ValueError("row_starts must be (T,)")
+    if out_scores is None:
+        out_scores = torch.empty((T, K), dtype=torch.float32, device=dev)
+    if out_ids is None:
+        out_ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    _check(out_scores, "out_scores", torch.float32, dev)
+    _check(out_ids, "out_ids", torch.int32, dev)
+    if out_ids.shape != (T, K) or out_scores.shape != (T, K):
+        raise ValueError("outputs must be (T, K)")
+    with torch.cuda.device(dev):
+        st = dcp_fused_topk(logits.data_ptr(), T, dcp, L, ld, K,
+                            None if row_starts is None else row_starts.data_ptr(),
+                            out_scores.data_ptr(), out_ids.data_ptr(), _stream_handle(stream))
+    if st != DCP_OK:
+        raise DcpError(st, "dcp_fused_topk")
     return out_scores, out_ids

@@ -60,17 +60,17 @@ struct MergeSource {
   // aligned bases).
   __host__ __device__ int staged_words() const { return 2 * dcp * K; }
 
-  template <int NT>
-  __device__ void issue(int t, uint32_t* dst) const {
-    const int n = dcp * K;
+  // One thread: arm `bar` with the row's bytes and copy row t's scores then
+  // ids into dst (needs K % 4 == 0 and 16-byte aligned bases).
+  __device__ void issue_tma(int t, uint32_t* dst, unsigned long long* bar) const {
+    const uint32_t seg = (uint32_t)K * 4u;
+    mbar_expect_tx(bar, 2u * (uint32_t)dcp * seg);
     const size_t stride = (size_t)T * (size_t)K;
     const float* sp = scores + (size_t)t * (size_t)K;
     const int32_t* ip = ids + (size_t)t * (size_t)K;
     for (int r = 0; r < dcp; ++r, sp += stride, ip += stride) {
-      for (int kk = 4 * (int)threadIdx.x; kk < K; kk += 4 * NT) {
-        cp_async16(dst + r * K + kk, sp + kk);
-        cp_async16(dst + n + r * K + kk, ip + kk);
-      }
+      tma_load_1d(dst + r * K, sp, seg, bar);
+      tma_load_1d(dst + dcp * K + r * K, ip, seg, bar);
     }
   }
 
@@ -150,10 +150,9 @@ struct LocalSource {
 
   __host__ __device__ int staged_words() const { return L; }
 
-  template <int NT>
-  __device__ void issue(int t, uint32_t* dst) const {
-    const float* row = logits + (size_t)t * (size_t)ld;
-    for (int c = threadIdx.x; c < (L >> 2); c += NT) cp_async16(dst + 4 * c, row + 4 * c);
+  __device__ void issue_tma(int t, uint32_t* dst, unsigned long long* bar) const {
+    mbar_expect_tx(bar, (uint32_t)L * 4u);
+    tma_load_1d(dst, logits + (size_t)t * (size_t)ld, (uint32_t)L * 4u, bar);
   }
 
   __device__ uint32_t inv(const uint32_t*, int i) const { return ~(uint32_t)i; }
@@ -186,6 +185,68 @@ struct LocalSource {
                           (uint32_t)rank * (uint32_t)L;
     return (int32_t)(base + c);
   }
+};
+
+// All dcp shards' logits of a row at once: candidate i = r*L + c is column c
+// of shard r's row (logits rank-major (dcp, T, ld)), global id
+// row_starts[t] + r*L + c.  By the composition of the local top-K and the
+// merge, the result equals merging the shards' local top-K.
+struct FusedSource {
+  const float* logits;
+  const int32_t* row_starts;
+  int T, dcp, L, ld;
+  bool vec4;
+
+  __device__ int count() const { return dcp * L; }
+
+  __device__ const float* row(int t, int r) const {
+    return logits + ((size_t)r * T + t) * (size_t)ld;
+  }
+
+  __device__ void stage(int t, uint32_t* skey, uint32_t* sinv) const {
+    for (int r = 0; r < dcp; ++r) {
+      const float* rp = row(t, r);
+      for (int c = threadIdx.x; c < L; c += kThreads) {
+        skey[r * L + c] = score_key(__float_as_uint(__ldg(rp + c)));
+        sinv[r * L + c] = ~(uint32_t)(r * L + c);
+      }
+    }
+  }
+
+  __host__ __device__ int staged_words() const { return dcp * L; }
+
+  __device__ void issue_tma(int t, uint32_t* dst, unsigned long long* bar) const {
+    const uint32_t seg = (uint32_t)L * 4u;
+    mbar_expect_tx(bar, (uint32_t)dcp * seg);
+    for (int r = 0; r < dcp; ++r) tma_load_1d(dst + r * L, row(t, r), seg, bar);
+  }
+
+  __device__ uint32_t inv(const uint32_t*, int i) const { return ~(uint32_t)i; }
+
+  __device__ uint4 inv4(const uint32_t*, int c) const {
+    const uint32_t i = 4u * (uint32_t)c;
+    return make_uint4(~i, ~(i + 1u), ~(i + 2u), ~(i + 3u));
+  }
+
+  __device__ uint32_t row_base(int t) const {
+    return row_starts ? (uint32_t)__ldg(row_starts + t) : 0u;
+  }
+
+  __device__ void prefetch_l2(int t) const {
+    for (int r = 0; r < dcp; ++r) prefetch_l2_bulk(row(t, r), (uint32_t)L * 4u);
+  }
+
+  __device__ uint32_t key_global(int t, int i) const {
+    const int r = i / L;
+    return score_key(__float_as_uint(__ldg(row(t, r) + (i - r * L))));
+  }
+  __device__ uint32_t inv_global(int, int i) const { return ~(uint32_t)i; }
+
+  __device__ int32_t out_id_from(uint32_t base, uint32_t inv) const {
+    return (int32_t)(base + ~inv);
+  }
+
+  __device__ int32_t out_id(int t, uint32_t inv) const { return out_id_from(row_base(t), inv); }
 };
 
 __host__ __device__ inline int next_pow2(int x) {
@@ -283,10 +344,31 @@ static cudaError_t device_info(DeviceInfo** out) {
     const int smem = d.max_smem_optin;
     if ((e = allow_max_smem(topk_rows_kernel<MergeSource>, smem)) != cudaSuccess) return e;
     if ((e = allow_max_smem(topk_rows_kernel<LocalSource>, smem)) != cudaSuccess) return e;
-    if ((e = allow_max_smem(topk_stream_kernel<512, MergeSource>, smem)) != cudaSuccess) return e;
-    if ((e = allow_max_smem(topk_stream_kernel<1024, MergeSource>, smem)) != cudaSuccess) return e;
-    if ((e = allow_max_smem(topk_stream_kernel<512, LocalSource>, smem)) != cudaSuccess) return e;
-    if ((e = allow_max_smem(topk_stream_kernel<1024, LocalSource>, smem)) != cudaSuccess) return e;
+    if ((e = allow_max_smem(topk_rows_kernel<FusedSource>, smem)) != cudaSuccess) return e;
+    if ((e = allow_max_smem(topk_stream_kernel<512, kStreamMaxN, MergeSource>, smem)) != cudaSuccess)
+      return e;
+    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxN, MergeSource>, smem)) !=
+        cudaSuccess)
+      return e;
+    if ((e = allow_max_smem(topk_stream_kernel<512, kStreamMaxN, LocalSource>, smem)) != cudaSuccess)
+      return e;
+    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxN, LocalSource>, smem)) !=
+        cudaSuccess)
+      return e;
+    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxNWide, FusedSource>, smem)) !=
+        cudaSuccess)
+      return e;
+    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxNWide, MergeSource>, smem)) !=
+        cudaSuccess)
+      return e;
+    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxNWide, LocalSource>, smem)) !=
+        cudaSuccess)
+      return e;
+    if ((e = allow_max_smem(topk_stream_kernel<512, kStreamMaxN, FusedSource>, smem)) != cudaSuccess)
+      return e;
+    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxN, FusedSource>, smem)) !=
+        cudaSuccess)
+      return e;
     d.configured = true;
   }
   *out = &d;
@@ -294,6 +376,29 @@ static cudaError_t device_info(DeviceInfo** out) {
 }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Device status word: kernels set bits here on failures they detect (a
+// staging copy that never completed); read and cleared by
+// dcp_topk_device_status.
+__device__ unsigned int g_device_status;
+
+static cudaError_t status_word(unsigned int** out) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_device_status);
+}
+
+// A kernel whose row copy is armed but never issued: exercises the bounded
+// wait and the status report.
+__global__ void wait_timeout_selftest_kernel(unsigned long long limit, unsigned int* status) {
+  __shared__ unsigned long long bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1u);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_expect_tx(&bar, 16u);
+  const bool ok = mbar_wait_bounded(&bar, 0u, limit);
+  if (__syncthreads_or(!ok) && threadIdx.x == 0) atomicOr(status, kStatusCopyTimeout);
+}
 
 // Streaming path when the row fits it (n <= 8192, K <= 2048, 16-byte copies
 // possible): one 1024-thread CTA per row when the rows fit on the SMs at
@@ -306,12 +411,25 @@ static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out
   if (device_info(&d) != cudaSuccess) return DCP_ERR_CUDA;
   const int words = src.staged_words();
   const size_t smem = stream_smem_bytes(words);
-  if (src.vec4 && n <= kStreamMaxN && K <= kStreamMaxK && smem <= (size_t)d->max_smem_optin) {
+  const bool stream_ok =
+      src.vec4 && K <= kStreamMaxK && smem <= (size_t)d->max_smem_optin && n <= kStreamMaxNWide;
+  if (stream_ok && n > kStreamMaxN) {
+    // up to 16384 candidates per row: one 1024-thread CTA per SM
+    unsigned int* status = nullptr;
+    if (status_word(&status) != cudaSuccess) return DCP_ERR_CUDA;
+    const int grid = T < d->sms ? T : d->sms;
+    topk_stream_kernel<1024, kStreamMaxNWide, Source>
+        <<<grid, 1024, smem, stream>>>(src, T, K, out_scores, out_ids, status);
+  } else if (stream_ok) {
+    unsigned int* status = nullptr;
+    if (status_word(&status) != cudaSuccess) return DCP_ERR_CUDA;
     if (T <= d->sms) {
-      topk_stream_kernel<1024, Source><<<T, 1024, smem, stream>>>(src, T, K, out_scores, out_ids);
+      topk_stream_kernel<1024, kStreamMaxN, Source>
+          <<<T, 1024, smem, stream>>>(src, T, K, out_scores, out_ids, status);
     } else {
       const int grid = T < 2 * d->sms ? T : 2 * d->sms;
-      topk_stream_kernel<512, Source><<<grid, 512, smem, stream>>>(src, T, K, out_scores, out_ids);
+      topk_stream_kernel<512, kStreamMaxN, Source>
+          <<<grid, 512, smem, stream>>>(src, T, K, out_scores, out_ids, status);
     }
   } else {
     const size_t gsmem = row_smem_bytes(n, K);
@@ -358,6 +476,39 @@ dcp_status dcp_local_topk(const float* logits, int T, int L, int ld, int K, int 
   dcp::LocalSource src{logits, row_starts, L, ld, rank,
                        (L % 4) == 0 && (ld % 4) == 0 && dcp::aligned16(logits)};
   return dcp::launch_rows(src, T, L, K, out_scores, out_ids, (cudaStream_t)stream);
+}
+
+dcp_status dcp_fused_topk(const float* logits, int T, int dcp_, int L, int ld, int K,
+                          const int32_t* row_starts, float* out_scores, int32_t* out_ids,
+                          dcp_stream_t stream) {
+  if (T < 0 || dcp_ < 1 || L < 1 || ld < L || K < 1) return DCP_ERR_INVALID;
+  if (K > DCP_MAX_K || (long long)dcp_ * L > DCP_MAX_CANDIDATES) return DCP_ERR_UNSUPPORTED;
+  if (T == 0) return DCP_OK;
+  if (!logits || !out_scores || !out_ids) return DCP_ERR_INVALID;
+  dcp::FusedSource src{logits, row_starts, T, dcp_, L, ld,
+                       (L % 4) == 0 && (ld % 4) == 0 && dcp::aligned16(logits)};
+  return dcp::launch_rows(src, T, dcp_ * L, K, out_scores, out_ids, (cudaStream_t)stream);
+}
+
+dcp_status dcp_topk_device_status(unsigned int* status) {
+  if (!status) return DCP_ERR_INVALID;
+  unsigned int* word = nullptr;
+  if (dcp::status_word(&word) != cudaSuccess) return DCP_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return DCP_ERR_CUDA;
+  unsigned int v = 0u;
+  if (cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return DCP_ERR_CUDA;
+  const unsigned int zero = 0u;
+  if (cudaMemcpy(word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return DCP_ERR_CUDA;
+  *status = v;
+  return DCP_OK;
+}
+
+dcp_status dcp_topk_selftest_wait_timeout(unsigned int wait_cycles, dcp_stream_t stream) {
+  unsigned int* word = nullptr;
+  if (dcp::status_word(&word) != cudaSuccess) return DCP_ERR_CUDA;
+  dcp::wait_timeout_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(wait_cycles, word);
+  return cudaGetLastError() == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
 }
 
 const char* dcp_status_string(dcp_status status) {

@@ -37,19 +37,24 @@
 // resetting shared state that late warps had not yet read).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 
 #include "topk_core.cuh"
 
 namespace dcp {
 
-constexpr int kStreamMaxN = 8192;             // candidates per row
+constexpr int kStreamMaxN = 8192;             // candidates per row (two CTAs per SM)
+constexpr int kStreamMaxNWide = 16384;        // candidates per row (one CTA per SM)
 constexpr int kStreamMaxK = 2048;
 constexpr int kLiveMax = 3072;                // live candidates per row
 constexpr int kFineMax = kStreamMaxK + 1024;  // fine buckets per row (bound, see SCAN1)
 constexpr int kArrSlack = 256;                // room past K for the bucket straddling K
 constexpr uint32_t kBigBucket = 64;           // larger buckets send the row to the fallback
+constexpr int kBigMax = (kStreamMaxK + (int)kBigBucket) / 5 + 1;  // such buckets starting before K
 constexpr uint32_t kNone = 0xFFFFFFFFu;
+constexpr unsigned long long kStageWaitLimit = 1ull << 31;  // cycles (about 1 s) to wait for a row's copy
+constexpr uint32_t kStatusCopyTimeout = 1u;     // device status bit: a staging copy timed out
 
 struct StreamShared {
   unsigned long long live[kLiveMax];  // live keys; then in bucket order; fallback: sorted winners
@@ -69,20 +74,69 @@ struct StreamShared {
   uint32_t above_b1;                  // candidates in bins above b1
   uint32_t found_digit, found_above, found_count;  // refinement of b1
   uint32_t p_end;                     // end of the bucket straddling K
+  uint32_t big[kBigMax];              // buckets of 5..kBigBucket keys starting before K: start << 8 | size
+  uint32_t nbig;
   uint32_t overflow;                  // a bucket to rank is too large, or does not fit the list
+  unsigned long long stage_bar;       // completes when a row's copies into the stage land
 };
+// 16-byte vector accesses to these arrays need 16-byte aligned offsets.
+static_assert(offsetof(StreamShared, live) % 16 == 0, "live must be 16-byte aligned");
+static_assert(offsetof(StreamShared, fine) % 16 == 0, "fine must be 16-byte aligned");
+static_assert(offsetof(StreamShared, u) % 16 == 0, "table must be 16-byte aligned");
+static_assert(offsetof(StreamShared, stage_bar) % 8 == 0, "mbarrier must be 8-byte aligned");
 
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem_src) : "memory");
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
+
+// mbarrier and 1-D bulk-copy (TMA) primitives.  One thread arms the barrier
+// with the byte count of a row and issues the row's copies; every thread then
+// waits on the barrier's phase.
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
 }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+// Copies `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global to shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_1d(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                            unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Waits for phase `parity` of `bar` to complete, giving up once `limit`
+// SM clock cycles have passed (each poll returns within a bounded time, so
+// the wait is bounded).  Returns whether the phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity,
+                                                  unsigned long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = clock64();
+  while (clock64() - t0 < limit)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
 // Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* gmem, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(gmem), "r"(bytes) : "memory");
@@ -156,6 +210,28 @@ inline size_t stream_smem_bytes(int words) {
   return ((sizeof(StreamShared) + 15) & ~(size_t)15) + (size_t)((words + 3) & ~3) * 4;
 }
 
+__device__ __forceinline__ void cas_desc(unsigned long long& x, unsigned long long& y) {
+  const bool sw = y > x;
+  const unsigned long long hi = sw ? y : x;
+  y = sw ? x : y;
+  x = hi;
+}
+
+// The n <= 8 keys at b sorted descending into a[0..n) (a 19-comparator
+// network; the absent keys are 0 and sort last).
+__device__ __forceinline__ void sort8_desc(const unsigned long long* b, uint32_t n,
+                                           unsigned long long (&a)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = (uint32_t)i < n ? b[i] : 0ull;
+  cas_desc(a[0], a[1]); cas_desc(a[2], a[3]); cas_desc(a[4], a[5]); cas_desc(a[6], a[7]);
+  cas_desc(a[0], a[2]); cas_desc(a[1], a[3]); cas_desc(a[4], a[6]); cas_desc(a[5], a[7]);
+  cas_desc(a[1], a[2]); cas_desc(a[5], a[6]); cas_desc(a[0], a[4]); cas_desc(a[3], a[7]);
+  cas_desc(a[1], a[5]); cas_desc(a[2], a[6]);
+  cas_desc(a[1], a[4]); cas_desc(a[3], a[6]);
+  cas_desc(a[2], a[4]); cas_desc(a[3], a[5]);
+  cas_desc(a[3], a[4]);
+}
+
 // Zeroes `words` (a multiple of 4) 16-byte-aligned shared words.
 template <int NT>
 __device__ __forceinline__ void zero_words(uint32_t* p, int words) {
@@ -163,12 +239,12 @@ __device__ __forceinline__ void zero_words(uint32_t* p, int words) {
     *reinterpret_cast<uint4*>(p + i) = make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <int NT, class Source>
+template <int NT, int MAXN, class Source>
 __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     topk_stream_kernel(Source src, int T, int K, float* __restrict__ out_scores,
-                       int32_t* __restrict__ out_ids) {
+                       int32_t* __restrict__ out_ids, unsigned int* __restrict__ status) {
   constexpr int kWarpsT = NT / 32;
-  constexpr int kVec = kStreamMaxN / 4 / NT;  // 16-byte score chunks per thread
+  constexpr int kVec = MAXN / 4 / NT;  // 16-byte score chunks per thread
   constexpr int kItems = 4 * kVec;
   constexpr int kLivePer = kLiveMax / NT;
   constexpr int kFinePer = kFineMax / NT;
@@ -178,7 +254,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   StreamShared& s = *reinterpret_cast<StreamShared*>(smem_raw);
   uint32_t* stage =
       reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(StreamShared) + 15) & ~(size_t)15));
-  const int n = src.count();  // multiple of 4, <= kStreamMaxN
+  const int n = src.count();  // multiple of 4, <= MAXN
   const int n4 = n >> 2;
   const int ksel = K < n ? K : n;
   const int tid = threadIdx.x;
@@ -188,6 +264,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   zero_words<NT>(s.fine, kFineMax);
   if (tid == 0) {
     s.live_cursor = 0u;
+    s.nbig = 0u;
     s.overflow = 0u;
     s.stat_or[0] = s.stat_or[1] = 0u;
     s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
@@ -198,13 +275,26 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   // visits exactly this sequence.
   const int G = (int)gridDim.x;
   int t = (int)blockIdx.x;
-  if (t < T) src.template issue<NT>(t, stage);
-  cp_async_commit();
-  if (tid == 0 && t + G < T) src.prefetch_l2(t + G);
+  if (tid == 0) {
+    mbar_init(&s.stage_bar, 1u);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    if (t < T) src.issue_tma(t, stage, &s.stage_bar);
+    if (t + G < T) src.prefetch_l2(t + G);
+  }
 
-  for (; t < T; t += G) {
-    cp_async_wait<0>();
-    __syncthreads();  // the row is staged and the previous row's state reset
+  for (uint32_t k = 0; t < T; t += G, ++k) {
+    const bool staged = mbar_wait_bounded(&s.stage_bar, k & 1u, kStageWaitLimit);
+    // the row is staged (or its copy timed out) and the previous row's state reset
+    if (__syncthreads_or(!staged)) {
+      // Report the timeout and stop this CTA; first give the copy a last,
+      // bounded chance to land so no copy is left writing into shared memory.
+      if (tid == 0) atomicOr(status, kStatusCopyTimeout);
+      mbar_wait_bounded(&s.stage_bar, k & 1u, kStageWaitLimit);
+      return;
+    }
     // Rows stream from HBM into L2 two rows ahead of their use; the copy of
     // the next row into shared memory starts as soon as this row's staged
     // data is consumed (after COMPACT).
@@ -322,8 +412,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     __syncthreads();
     // The staged row is consumed (the fallback re-reads its row from global
     // memory): stream the next row in behind the rest of this one.
-    if (t + G < T) src.template issue<NT>(t + G, stage);
-    cp_async_commit();
+    if (tid == 0 && t + G < T) src.issue_tma(t + G, stage, &s.stage_bar);
 
     // ---- L2: live keys into registers; which bits vary over them ----------
     unsigned long long lkey[kLivePer];
@@ -419,10 +508,11 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         if (g < nfine) {
           s.fine[g] = st << 16;
           if (st < (uint32_t)ksel) {
-            // the list holds ksel + kArrSlack keys; ranking is quadratic
-            // in a bucket's size
+            // the list holds ksel + kArrSlack keys; buckets of more than 4
+            // keys are sorted whole from a list of their own
             if (st + c[e] > (uint32_t)(ksel + kArrSlack) || c[e] > kBigBucket) over = 1u;
             if ((uint32_t)ksel <= st + c[e]) s.p_end = st + c[e];
+            if (c[e] > 4u) s.big[atomicAdd(&s.nbig, 1u) % (uint32_t)kBigMax] = (st << 8) | c[e];
           }
           st += c[e];
         }
@@ -461,28 +551,52 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         const unsigned long long mine = s.live[p];
         const uint32_t meta = s.fine[bucket_of[p]];
         const uint32_t st = meta >> 16, cnt = meta & 0xFFFFu;
+        if (cnt > 4u) continue;  // ordered from the list of larger buckets below
         uint32_t fin = p;
         if (cnt > 1u) {
+          // the bucket lies within [p - 3, p + 3]: members before p rank
+          // above it when not smaller, members after it when larger
           uint32_t r = 0u;
-          if (cnt <= 4u) {
-            // the bucket lies within [p - 3, p + 3]: members before p rank
-            // above it when not smaller, members after it when larger
 #pragma unroll
-            for (int d = 1; d <= 3; ++d) {
-              if (p - (uint32_t)d - st < cnt) r += s.live[p - d] >= mine ? 1u : 0u;
-              if (p + (uint32_t)d - st < cnt) r += s.live[p + d] > mine ? 1u : 0u;
-            }
-          } else {
-            for (uint32_t e = st; e < st + cnt; ++e) {
-              const unsigned long long o = s.live[e];
-              r += (o > mine || (e < p && o == mine)) ? 1u : 0u;
-            }
+          for (int d = 1; d <= 3; ++d) {
+            if (p - (uint32_t)d - st < cnt) r += s.live[p - d] >= mine ? 1u : 0u;
+            if (p + (uint32_t)d - st < cnt) r += s.live[p + d] > mine ? 1u : 0u;
           }
           fin = st + r;
         }
         if (fin < (uint32_t)ksel) {
           os[fin] = __uint_as_float(score_bits((uint32_t)(mine >> 32)));
           oi[fin] = src.out_id_from(rbase, (uint32_t)mine);
+        }
+      }
+      const int nbig = min((int)s.nbig, kBigMax);
+      for (int i = tid; i < nbig; i += NT) {
+        const uint32_t ent = s.big[i];
+        const uint32_t st = ent >> 8, cnt = ent & 0xFFu;
+        const uint32_t nout = min(cnt, (uint32_t)ksel - st);
+        if (cnt <= 8u) {
+          unsigned long long a[8];
+          sort8_desc(s.live + st, cnt, a);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if ((uint32_t)j < nout) {
+              os[st + j] = __uint_as_float(score_bits((uint32_t)(a[j] >> 32)));
+              oi[st + j] = src.out_id_from(rbase, (uint32_t)a[j]);
+            }
+          }
+        } else {
+          for (uint32_t m = 0; m < cnt; ++m) {
+            const unsigned long long mine = s.live[st + m];
+            uint32_t r = 0u;
+            for (uint32_t e = 0; e < cnt; ++e) {
+              const unsigned long long o = s.live[st + e];
+              r += (o > mine || (e < m && o == mine)) ? 1u : 0u;
+            }
+            if (r < nout) {
+              os[st + r] = __uint_as_float(score_bits((uint32_t)(mine >> 32)));
+              oi[st + r] = src.out_id_from(rbase, (uint32_t)mine);
+            }
+          }
         }
       }
       for (int j = ksel + tid; j < K; j += NT) {
@@ -514,12 +628,12 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     zero_words<NT>(s.fine, kFineMax);
     if (tid == 0) {
       s.live_cursor = 0u;
+      s.nbig = 0u;
       s.overflow = 0u;
       s.stat_or[0] = s.stat_or[1] = 0u;
       s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
     }
   }
-  cp_async_wait<0>();
 }
 
 }  // namespace dcp

@@ -88,3 +88,21 @@ def test_merge_argument_errors(args, want):
 ])
 def test_local_argument_errors(args, want):
     assert dk.dcp_local_topk(*args, None) == want
+
+
+def test_device_status_rejects_null():
+    assert dk.library().dcp_topk_device_status(None) == dk.DCP_ERR_INVALID
+
+
+@pytest.mark.parametrize("args,want", [
+    ((FAKE, -1, 4, 8, 8, 4, None, FAKE, FAKE), dk.DCP_ERR_INVALID),
+    ((FAKE, 2, 0, 8, 8, 4, None, FAKE, FAKE), dk.DCP_ERR_INVALID),
+    ((FAKE, 2, 4, 8, 7, 4, None, FAKE, FAKE), dk.DCP_ERR_INVALID),
+    ((FAKE, 2, 4, 8, 8, 0, None, FAKE, FAKE), dk.DCP_ERR_INVALID),
+    ((None, 2, 4, 8, 8, 4, None, FAKE, FAKE), dk.DCP_ERR_INVALID),
+    ((FAKE, 2, 5, 4096, 4096, 4, None, FAKE, FAKE), dk.DCP_ERR_UNSUPPORTED),
+    ((FAKE, 2, 4, 8, 8, 4097, None, FAKE, FAKE), dk.DCP_ERR_UNSUPPORTED),
+    ((None, 0, 4, 8, 8, 4, None, None, None), dk.DCP_OK),
+])
+def test_fused_argument_errors(args, want):
+    assert dk.dcp_fused_topk(*args, None) == want

@@ -233,3 +233,57 @@ def test_sweep_local_then_merge(T):
     for r in range(dcp):
         ls, li = oracle.local_topk(logits[r], K, r, dcp)
         assert_same((cand_i[r].cpu().numpy(), cand_s[r].cpu().numpy()), (li, ls), f"local r={r}")
+
+
+def test_staging_wait_timeout_reports_status():
+    """The bounded wait on a row's copy barrier gives up and reports it: a
+    self-test kernel arms the barrier for a copy it never issues.  The
+    context stays usable afterwards."""
+    assert dk.dcp_topk_device_status() == 0
+    assert dk.dcp_topk_selftest_wait_timeout(200000, torch.cuda.current_stream().cuda_stream) == dk.DCP_OK
+    assert dk.dcp_topk_device_status() == dk.DCP_DEVICE_COPY_TIMEOUT
+    assert dk.dcp_topk_device_status() == 0  # read clears it
+    m = workloads.decode(seed=5, T=3)
+    assert_same(run_merge(m), oracle.merge(m.scores, m.ids), "after timeout")
+    assert dk.dcp_topk_device_status() == 0
+
+
+def test_no_device_status_after_runs():
+    m = workloads.prefill(T=400)
+    run_merge(m)
+    assert dk.dcp_topk_device_status() == 0
+
+
+FUSED_CASES = [
+    # (T, dcp, L, ld, K, mode)
+    (4, 4, 4096, 4096, 2048, "bf16"),
+    (3, 4, 4096, 4100, 2048, "normal"),
+    (5, 2, 1000, 1000, 64, "ties"),
+    (2, 3, 1001, 1003, 200, "normal"),
+    (2, 2, 60, 60, 200, "bf16"),       # fewer candidates than K: padded
+    (160, 4, 4096, 4096, 2048, "bf16"),  # more rows than SMs
+    (3, 8, 2048, 2048, 2048, "ties"),
+]
+
+
+@pytest.mark.parametrize("case", FUSED_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_fused_topk(case):
+    """Top-K over all shards' logits in one call equals the oracle's fused
+    top-K (and so, by the pinned composition identity, local top-K + merge)."""
+    T, dcp, L, ld, K, mode = case
+    seed = zlib.crc32(repr(case).encode()) & 0xFFFF
+    logits = np.stack([workloads.random_logits(seed + r, T, L, ld=ld, mode=mode) for r in range(dcp)])
+    rs = (np.arange(T, dtype=np.int32) * 5) if T % 2 else None
+    out_s, out_i = dk.fused_topk(_dev(logits), K, L=L, row_starts=None if rs is None else _dev(rs))
+    torch.cuda.synchronize()
+    want_s, want_i = oracle.fused_topk(logits, K, L=L, row_starts=rs)
+    assert_same((out_i.cpu().numpy(), out_s.cpu().numpy()), (want_i, want_s), str(case))
+
+
+@pytest.mark.parametrize("T", workloads.SWEEP_T)
+def test_sweep_fused(T):
+    logits = workloads.sweep_logits(T)
+    out_s, out_i = dk.fused_topk(_dev(logits), 2048)
+    torch.cuda.synchronize()
+    want_s, want_i = oracle.fused_topk(logits, 2048)
+    assert_same((out_i.cpu().numpy(), out_s.cpu().numpy()), (want_i, want_s), f"T={T}")
