@@ -5,7 +5,7 @@
 // A persistent grid walks the rows: CTAs of 512 threads, two per SM, for many
 // rows (one CTA's row streams in from HBM while the other CTA selects), or one
 // 1024-thread CTA per row for a few rows.  A row is staged in shared memory
-// with 16-byte cp.async copies read straight from the rank-major layout, and
+// by bulk copies (TMA) read straight from the rank-major layout, and
 // selection and final order come out of one two-level bucket pass instead of
 // a radix select followed by a sort:
 //
@@ -29,8 +29,8 @@
 //
 // Rows whose live set or buckets come out too large for this (pathologically
 // clustered keys) take the radix-select + sort of topk_core.cuh on the same
-// staged row: the result never depends on the data's distribution, only the
-// speed does.
+// row (read again from global memory): the result never depends on the
+// data's distribution, only the speed does.
 //
 // Barriers: shared state is reset only after the barrier that follows its last
 // reader in the row (the race the first page's review reports came from
@@ -65,8 +65,8 @@ struct StreamShared {
   } u;
   uint32_t wa[kMaxWarps];
   uint32_t wb[kMaxWarps];
-  uint32_t stat_or[2];                // over live finite candidates: low 21 score bits, ~id
-  uint32_t stat_and[2];
+  uint32_t stat_or[2];                // OR of the raw scores' low 21 bits; OR of ~ids (not 0)
+  uint32_t stat_and[2];               // [1]: AND of ~ids (not 0)
   uint32_t live_cursor;
   uint32_t b1;                        // L1 bin of the K-th largest key
   uint32_t nlive;                     // candidates in bins >= b1
@@ -301,12 +301,17 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     if (tid == 0 && t + 2 * G < T) src.prefetch_l2(t + 2 * G);
 
     // ---- L1: histogram of the score keys' top 11 bits ---------------------
+    // Also ORs the low 21 bits of every raw score: the bits that are zero in
+    // all of them are constant in every key of one sign (bf16-valued scores
+    // leave the low 16 zero), which the buckets below skip.
     uint32_t keys[kItems];
+    uint32_t raw_or = 0u;
 #pragma unroll
     for (int v = 0; v < kVec; ++v) {
       const int c = tid + v * NT;
       if (c < n4) {
         const uint4 w = *reinterpret_cast<const uint4*>(stage + 4 * c);
+        raw_or |= w.x | w.y | w.z | w.w;
         keys[4 * v + 0] = score_key(w.x);
         keys[4 * v + 1] = score_key(w.y);
         keys[4 * v + 2] = score_key(w.z);
@@ -318,6 +323,8 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         for (int e = 0; e < 4; ++e) keys[4 * v + e] = 0u;
       }
     }
+    raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & 0x1FFFFFu);
+    if (lane == 0 && raw_or) atomicOr(&s.stat_or[0], raw_or);
     __syncthreads();
 
     // ---- SCAN1: bins high to low; packed (buckets << 16 | candidates) -------
@@ -396,6 +403,10 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       uint32_t base = 0u;
       if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
       unsigned long long* dst = s.live + (__shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt);
+      // OR / AND of the inverted ids around the live candidates (padding's
+      // ~id of 0 left out: it is the smallest, so ordering on the varying
+      // bits alone still puts it last)
+      uint32_t ior = 0u, iand = 0xFFFFFFFFu;
 #pragma unroll
       for (int v = 0; v < kVec; ++v) {
         if ((mask >> (4 * v)) & 0xFu) {
@@ -403,10 +414,18 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
           const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
+            ior |= us[e];
+            iand &= us[e] ? us[e] : 0xFFFFFFFFu;
             if (mask & (1u << (4 * v + e)))
               *dst++ = ((unsigned long long)keys[4 * v + e] << 32) | us[e];
           }
         }
+      }
+      ior = __reduce_or_sync(0xFFFFFFFFu, ior);
+      iand = __reduce_and_sync(0xFFFFFFFFu, iand);
+      if (lane == 0) {
+        atomicOr(&s.stat_or[1], ior);
+        atomicAnd(&s.stat_and[1], iand);
       }
     }
     __syncthreads();
@@ -414,54 +433,29 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     // memory): stream the next row in behind the rest of this one.
     if (tid == 0 && t + G < T) src.issue_tma(t + G, stage, &s.stage_bar);
 
-    // ---- L2: live keys into registers; which bits vary over them ----------
+    // ---- L2: fine bucket of every live candidate ---------------------------
     unsigned long long lkey[kLivePer];
     uint32_t gslot[kLivePer];
     if (fast) {
-      uint32_t lor = 0u, land = 0xFFFFFFFFu, ior = 0u, iand = 0xFFFFFFFFu;
-#pragma unroll
-      for (int u = 0; u < kLivePer; ++u) {
-        const int e = tid + u * NT;
-        lkey[u] = e < nlive ? s.live[e] : 0ull;
-        const uint32_t k = (uint32_t)(lkey[u] >> 32);
-        if (e < nlive && (k >> 21) > 3u) {  // finite score
-          const uint32_t lo = ((k & 0x80000000u) ? k : ~k) & 0x1FFFFFu;
-          lor |= lo;
-          land &= lo;
-          ior |= (uint32_t)lkey[u];
-          iand &= (uint32_t)lkey[u];
-        }
-      }
-      lor = __reduce_or_sync(0xFFFFFFFFu, lor);
-      land = __reduce_and_sync(0xFFFFFFFFu, land);
-      ior = __reduce_or_sync(0xFFFFFFFFu, ior);
-      iand = __reduce_and_sync(0xFFFFFFFFu, iand);
-      if (lane == 0) {
-        atomicOr(&s.stat_or[0], lor);
-        atomicAnd(&s.stat_and[0], land);
-        atomicOr(&s.stat_or[1], ior);
-        atomicAnd(&s.stat_and[1], iand);
-      }
-    }
-    __syncthreads();
-
-    // ---- L2: fine bucket of every live candidate ---------------------------
-    if (fast) {
-      // For finite scores: the low 21 key bits below tzf, and the bits of ~id
-      // at or above ibf, are equal for every live candidate, so within one bin
-      // keys are ordered like y = (low key bits >> tzf) << ibf | (~id low ibf
-      // bits), a wf-bit number whose top q bits name the bucket.  Bins 0..3
-      // (-inf, where padding lives, and below) keep every bit (53).
-      const uint32_t vk = s.stat_or[0] ^ s.stat_and[0];
+      // For finite scores the low 21 key bits below tzf are equal within a
+      // sign, and the bits of ~id at or above ibf are equal for every live
+      // candidate (but padding), so within one bin keys are ordered like
+      // y = (low key bits >> tzf) << ibf | (~id low ibf bits), a wf-bit number
+      // whose top q bits name the bucket.  Bins 0..3 (-inf, where padding
+      // lives, and below) keep every bit (53).
+      const uint32_t ro = s.stat_or[0];
       const uint32_t vi = s.stat_or[1] ^ s.stat_and[1];
-      const int tzf = vk ? min(__ffs(vk) - 1, 21) : 21;
+      const int tzf = ro ? min(__ffs(ro) - 1, 21) : 21;
       const int ibf = vi ? 32 - __clz(vi) : 0;
       const uint32_t imask = ibf >= 32 ? 0xFFFFFFFFu : ((1u << ibf) - 1u);
       const int wf = 21 - tzf + ibf;
 #pragma unroll
       for (int u = 0; u < kLivePer; ++u) {
+        const int e = tid + u * NT;
         gslot[u] = kNone;
-        if (tid + u * NT < nlive) {
+        lkey[u] = 0ull;
+        if (e < nlive) {
+          lkey[u] = s.live[e];
           const uint32_t k = (uint32_t)(lkey[u] >> 32);
           const uint32_t inv = (uint32_t)lkey[u];
           const uint32_t bin = k >> 21;
@@ -604,7 +598,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         oi[j] = -1;
       }
     } else {
-      // ---- Fallback: radix select + sort on the staged row -----------------
+      // ---- Fallback: radix select + sort, reading the row from global memory -
       int n_pow2 = 1;
       while (n_pow2 < ksel) n_pow2 <<= 1;
       select_sort_row<NT>(
