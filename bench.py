@@ -360,10 +360,18 @@ def decode_and_sweep(torch, dk, dev, stream):
         def fn():
             dk.merge(s, i, out_ids=oi, out_scores=os_, stream=stream)
 
-        launch = median_of_reps(torch, fn, stream)
-        graph = median_of_reps(torch, fn, stream, graph=True)
-        out[f"{name}_T{m.T}_us_per_launch"] = launch
-        out[f"{name}_T{m.T}_us_per_graph_replay"] = graph
+        # the C ABI called with prepared arguments: the launch cost without
+        # the Python wrapper's checks
+        lib = dk.library()
+        args = (s.data_ptr(), i.data_ptr(), m.T, m.dcp, m.K, None, oi.data_ptr(),
+                os_.data_ptr(), None, 0, stream.cuda_stream)
+
+        def raw():
+            lib.dcp_topk_merge(*args)
+
+        out[f"{name}_T{m.T}_us_per_launch"] = median_of_reps(torch, raw, stream)
+        out[f"{name}_T{m.T}_us_per_graph_replay"] = median_of_reps(torch, raw, stream, graph=True)
+        out[f"{name}_T{m.T}_us_per_python_call"] = median_of_reps(torch, fn, stream)
     sweep = {}
     K = 2048
     for T in workloads.SWEEP_T:

@@ -5,6 +5,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "dcp_topk.h"
@@ -310,10 +311,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Device status word: kernels set bits here on failures they detect (a
+// staging copy that never completed); read and cleared by
+// dcp_topk_device_status.
+__device__ unsigned int g_device_status;
+
+static cudaError_t status_word(unsigned int** out) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_device_status);
+}
+
 struct DeviceInfo {
   int sms = 0;
   int max_smem_optin = 0;
-  bool configured = false;
+  unsigned int* status = nullptr;  // device address of g_device_status
+  std::atomic<bool> configured{false};
 };
 
 static DeviceInfo g_dev[64];
@@ -334,9 +345,13 @@ static cudaError_t device_info(DeviceInfo** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_dev_mutex);
   DeviceInfo& d = g_dev[dev];
-  if (!d.configured) {
+  if (d.configured.load(std::memory_order_acquire)) {
+    *out = &d;
+    return cudaSuccess;
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!d.configured.load(std::memory_order_relaxed)) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -369,22 +384,14 @@ static cudaError_t device_info(DeviceInfo** out) {
     if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxN, FusedSource>, smem)) !=
         cudaSuccess)
       return e;
-    d.configured = true;
+    if ((e = status_word(&d.status)) != cudaSuccess) return e;
+    d.configured.store(true, std::memory_order_release);
   }
   *out = &d;
   return cudaSuccess;
 }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-
-// Device status word: kernels set bits here on failures they detect (a
-// staging copy that never completed); read and cleared by
-// dcp_topk_device_status.
-__device__ unsigned int g_device_status;
-
-static cudaError_t status_word(unsigned int** out) {
-  return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_device_status);
-}
 
 // A kernel whose row copy is armed but never issued: exercises the bounded
 // wait and the status report.
@@ -415,14 +422,12 @@ static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out
       src.vec4 && K <= kStreamMaxK && smem <= (size_t)d->max_smem_optin && n <= kStreamMaxNWide;
   if (stream_ok && n > kStreamMaxN) {
     // up to 16384 candidates per row: one 1024-thread CTA per SM
-    unsigned int* status = nullptr;
-    if (status_word(&status) != cudaSuccess) return DCP_ERR_CUDA;
+    unsigned int* status = d->status;
     const int grid = T < d->sms ? T : d->sms;
     topk_stream_kernel<1024, kStreamMaxNWide, Source>
         <<<grid, 1024, smem, stream>>>(src, T, K, out_scores, out_ids, status);
   } else if (stream_ok) {
-    unsigned int* status = nullptr;
-    if (status_word(&status) != cudaSuccess) return DCP_ERR_CUDA;
+    unsigned int* status = d->status;
     if (T <= d->sms) {
       topk_stream_kernel<1024, kStreamMaxN, Source>
           <<<T, 1024, smem, stream>>>(src, T, K, out_scores, out_ids, status);

@@ -541,11 +541,29 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       // ---- RANK: in list order, position = bucket start + larger members ---
       const uint32_t p_end = s.p_end;
       const uint32_t rbase = src.row_base(t);
-      for (uint32_t p = tid; p < p_end; p += NT) {
-        const unsigned long long mine = s.live[p];
-        const uint32_t meta = s.fine[bucket_of[p]];
-        const uint32_t st = meta >> 16, cnt = meta & 0xFFFFu;
-        if (cnt > 4u) continue;  // ordered from the list of larger buckets below
+      // positions handled together, so their loads overlap
+      constexpr int kRankPer = (kStreamMaxK + kArrSlack + NT - 1) / NT;
+      unsigned long long mine[kRankPer];
+      uint32_t meta[kRankPer];
+#pragma unroll
+      for (int u = 0; u < kRankPer; ++u) {
+        const uint32_t p = tid + u * NT;
+        mine[u] = p < p_end ? s.live[p] : 0ull;
+        meta[u] = p < p_end ? (uint32_t)bucket_of[p] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kRankPer; ++u) {
+        const uint32_t p = tid + u * NT;
+        // bucket start << 16 | size; size 0 marks a position past the list
+        meta[u] = p < p_end ? s.fine[meta[u]] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kRankPer; ++u) {
+        const uint32_t p = tid + u * NT;
+        const uint32_t st = meta[u] >> 16, cnt = meta[u] & 0xFFFFu;
+        // empty slots, and buckets of more than 4 (ordered from their own
+        // list below), are skipped
+        if (cnt == 0u || cnt > 4u) continue;
         uint32_t fin = p;
         if (cnt > 1u) {
           // the bucket lies within [p - 3, p + 3]: members before p rank
@@ -553,14 +571,14 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
           uint32_t r = 0u;
 #pragma unroll
           for (int d = 1; d <= 3; ++d) {
-            if (p - (uint32_t)d - st < cnt) r += s.live[p - d] >= mine ? 1u : 0u;
-            if (p + (uint32_t)d - st < cnt) r += s.live[p + d] > mine ? 1u : 0u;
+            if (p - (uint32_t)d - st < cnt) r += s.live[p - d] >= mine[u] ? 1u : 0u;
+            if (p + (uint32_t)d - st < cnt) r += s.live[p + d] > mine[u] ? 1u : 0u;
           }
           fin = st + r;
         }
         if (fin < (uint32_t)ksel) {
-          os[fin] = __uint_as_float(score_bits((uint32_t)(mine >> 32)));
-          oi[fin] = src.out_id_from(rbase, (uint32_t)mine);
+          os[fin] = __uint_as_float(score_bits((uint32_t)(mine[u] >> 32)));
+          oi[fin] = src.out_id_from(rbase, (uint32_t)mine[u]);
         }
       }
       const int nbig = min((int)s.nbig, kBigMax);
