@@ -22,10 +22,13 @@
 //          numbered in key order, so a prefix sum over their sizes gives each
 //          bucket its first output position.
 //  RANK    a live candidate in a bucket that starts before K counts the bucket
-//          members with larger keys: its output position is the bucket start
-//          plus that count, and positions >= K are the losers.  Buckets hold a
-//          few members, so this one step both finishes the selection at the
-//          threshold and sorts the winners.
+//          members with larger keys (members of shared buckets are first
+//          gathered into the bucket's slice of the live list): its output
+//          position is the bucket start plus that count, and positions >= K
+//          are the losers.  Buckets hold a few members, so this one step both
+//          finishes the selection at the threshold and sorts the winners.  The
+//          row's output is assembled in shared memory and leaves in 16-byte
+//          stores.
 //
 // Rows whose live set or buckets come out too large for this (pathologically
 // clustered keys) take the radix-select + sort of topk_core.cuh on the same
@@ -49,9 +52,7 @@ constexpr int kStreamMaxNWide = 16384;        // candidates per row (one CTA per
 constexpr int kStreamMaxK = 2048;
 constexpr int kLiveMax = 3072;                // live candidates per row
 constexpr int kFineMax = kStreamMaxK + 1024;  // fine buckets per row (bound, see SCAN1)
-constexpr int kArrSlack = 256;                // room past K for the bucket straddling K
-constexpr uint32_t kBigBucket = 64;           // larger buckets send the row to the fallback
-constexpr int kBigMax = (kStreamMaxK + (int)kBigBucket) / 5 + 1;  // such buckets starting before K
+constexpr uint32_t kBigBucket = 255;          // a larger bucket starting before K sends the row to the fallback
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr unsigned long long kStageWaitLimit = 1ull << 31;  // cycles (about 1 s) to wait for a row's copy
 constexpr uint32_t kStatusCopyTimeout = 1u;     // device status bit: a staging copy timed out
@@ -73,16 +74,15 @@ struct StreamShared {
   uint32_t nfine;                     // fine buckets of bins >= b1
   uint32_t above_b1;                  // candidates in bins above b1
   uint32_t found_digit, found_above, found_count;  // refinement of b1
-  uint32_t p_end;                     // end of the bucket straddling K
-  uint32_t big[kBigMax];              // buckets of 5..kBigBucket keys starting before K: start << 8 | size
-  uint32_t nbig;
-  uint32_t overflow;                  // a bucket to rank is too large, or does not fit the list
+  uint32_t overflow;                  // a bucket to rank is too large
   unsigned long long stage_bar;       // completes when a row's copies into the stage land
 };
 // 16-byte vector accesses to these arrays need 16-byte aligned offsets.
 static_assert(offsetof(StreamShared, live) % 16 == 0, "live must be 16-byte aligned");
 static_assert(offsetof(StreamShared, fine) % 16 == 0, "fine must be 16-byte aligned");
-static_assert(offsetof(StreamShared, u) % 16 == 0, "table must be 16-byte aligned");
+static_assert(offsetof(StreamShared, u) == offsetof(StreamShared, fine) + sizeof(uint32_t) * kFineMax,
+              "the table must follow fine directly (one region for output staging and reset)");
+static_assert(2 * kStreamMaxK <= kFineMax + kHistBins, "output staging must fit fine + table");
 static_assert(offsetof(StreamShared, stage_bar) % 8 == 0, "mbarrier must be 8-byte aligned");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -210,28 +210,6 @@ inline size_t stream_smem_bytes(int words) {
   return ((sizeof(StreamShared) + 15) & ~(size_t)15) + (size_t)((words + 3) & ~3) * 4;
 }
 
-__device__ __forceinline__ void cas_desc(unsigned long long& x, unsigned long long& y) {
-  const bool sw = y > x;
-  const unsigned long long hi = sw ? y : x;
-  y = sw ? x : y;
-  x = hi;
-}
-
-// The n <= 8 keys at b sorted descending into a[0..n) (a 19-comparator
-// network; the absent keys are 0 and sort last).
-__device__ __forceinline__ void sort8_desc(const unsigned long long* b, uint32_t n,
-                                           unsigned long long (&a)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) a[i] = (uint32_t)i < n ? b[i] : 0ull;
-  cas_desc(a[0], a[1]); cas_desc(a[2], a[3]); cas_desc(a[4], a[5]); cas_desc(a[6], a[7]);
-  cas_desc(a[0], a[2]); cas_desc(a[1], a[3]); cas_desc(a[4], a[6]); cas_desc(a[5], a[7]);
-  cas_desc(a[1], a[2]); cas_desc(a[5], a[6]); cas_desc(a[0], a[4]); cas_desc(a[3], a[7]);
-  cas_desc(a[1], a[5]); cas_desc(a[2], a[6]);
-  cas_desc(a[1], a[4]); cas_desc(a[3], a[6]);
-  cas_desc(a[2], a[4]); cas_desc(a[3], a[5]);
-  cas_desc(a[3], a[4]);
-}
-
 // Zeroes `words` (a multiple of 4) 16-byte-aligned shared words.
 template <int NT>
 __device__ __forceinline__ void zero_words(uint32_t* p, int words) {
@@ -260,11 +238,9 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
 
-  zero_words<NT>(s.u.table, kHistBins);
-  zero_words<NT>(s.fine, kFineMax);
+  zero_words<NT>(s.fine, kFineMax + kHistBins);  // fine and the table behind it
   if (tid == 0) {
     s.live_cursor = 0u;
-    s.nbig = 0u;
     s.overflow = 0u;
     s.stat_or[0] = s.stat_or[1] = 0u;
     s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
@@ -480,6 +456,8 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     __syncthreads();
 
     // ---- SCAN2: bucket starts ------------------------------------------------
+    // fine[g] becomes start << 16 | min(size, 255) << 8, its low byte the
+    // fill cursor for SCATTER.
     if (fast) {
       uint32_t c[kFinePer];
       uint32_t local = 0u;
@@ -500,14 +478,8 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       for (int e = 0; e < kFinePer; ++e) {
         const int g = kFinePer * tid + e;
         if (g < nfine) {
-          s.fine[g] = st << 16;
-          if (st < (uint32_t)ksel) {
-            // the list holds ksel + kArrSlack keys; buckets of more than 4
-            // keys are sorted whole from a list of their own
-            if (st + c[e] > (uint32_t)(ksel + kArrSlack) || c[e] > kBigBucket) over = 1u;
-            if ((uint32_t)ksel <= st + c[e]) s.p_end = st + c[e];
-            if (c[e] > 4u) s.big[atomicAdd(&s.nbig, 1u) % (uint32_t)kBigMax] = (st << 8) | c[e];
-          }
+          s.fine[g] = (st << 16) | (min(c[e], 255u) << 8);
+          if (st < (uint32_t)ksel && c[e] > kBigBucket) over = 1u;
           st += c[e];
         }
       }
@@ -519,101 +491,52 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
 
     float* os = out_scores + (size_t)t * (size_t)K;
     int32_t* oi = out_ids + (size_t)t * (size_t)K;
+    // Output staging, once `fine` and the L1 table are no longer read: the
+    // row's scores in words [0, K), its ids in [K, 2K).
+    uint32_t* ostage = s.fine;
     if (fast) {
-      // ---- SCATTER: members of buckets starting before K, in bucket order --
-      // The L1 table is no longer read: it now holds, per list position, the
-      // bucket of the key there.
-      uint16_t* bucket_of = reinterpret_cast<uint16_t*>(s.u.table);
+      // ---- SCATTER: members of shared buckets starting before K ------------
+      // gslot[u] becomes the bucket's start << 16 | size << 8 | this key's
+      // slot in it (kNone for a key whose bucket starts at or after K).
 #pragma unroll
       for (int u = 0; u < kLivePer; ++u) {
         if (gslot[u] != kNone) {
           const uint32_t old = atomicAdd(&s.fine[gslot[u]], 1u);
-          const uint32_t st = old >> 16;
-          if (st < (uint32_t)ksel) {
-            const uint32_t pos = st + (old & 0xFFFFu);
-            s.live[pos] = lkey[u];
-            bucket_of[pos] = (uint16_t)gslot[u];
+          gslot[u] = kNone;
+          if ((old >> 16) < (uint32_t)ksel) {
+            gslot[u] = old;
+            if (((old >> 8) & 0xFFu) > 1u) s.live[(old >> 16) + (old & 0xFFu)] = lkey[u];
           }
         }
       }
       __syncthreads();
 
-      // ---- RANK: in list order, position = bucket start + larger members ---
-      const uint32_t p_end = s.p_end;
+      // ---- RANK: position = bucket start + members ranking above ----------
+      // A member ranks above another when its key is larger, or equal with
+      // a smaller slot (identical keys are interchangeable).
       const uint32_t rbase = src.row_base(t);
-      // positions handled together, so their loads overlap
-      constexpr int kRankPer = (kStreamMaxK + kArrSlack + NT - 1) / NT;
-      unsigned long long mine[kRankPer];
-      uint32_t meta[kRankPer];
 #pragma unroll
-      for (int u = 0; u < kRankPer; ++u) {
-        const uint32_t p = tid + u * NT;
-        mine[u] = p < p_end ? s.live[p] : 0ull;
-        meta[u] = p < p_end ? (uint32_t)bucket_of[p] : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < kRankPer; ++u) {
-        const uint32_t p = tid + u * NT;
-        // bucket start << 16 | size; size 0 marks a position past the list
-        meta[u] = p < p_end ? s.fine[meta[u]] : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < kRankPer; ++u) {
-        const uint32_t p = tid + u * NT;
-        const uint32_t st = meta[u] >> 16, cnt = meta[u] & 0xFFFFu;
-        // empty slots, and buckets of more than 4 (ordered from their own
-        // list below), are skipped
-        if (cnt == 0u || cnt > 4u) continue;
-        uint32_t fin = p;
+      for (int u = 0; u < kLivePer; ++u) {
+        const uint32_t en = gslot[u];
+        if (en == kNone) continue;
+        const uint32_t st = en >> 16, cnt = (en >> 8) & 0xFFu, slot = en & 0xFFu;
+        uint32_t r = 0u;
         if (cnt > 1u) {
-          // the bucket lies within [p - 3, p + 3]: members before p rank
-          // above it when not smaller, members after it when larger
-          uint32_t r = 0u;
-#pragma unroll
-          for (int d = 1; d <= 3; ++d) {
-            if (p - (uint32_t)d - st < cnt) r += s.live[p - d] >= mine[u] ? 1u : 0u;
-            if (p + (uint32_t)d - st < cnt) r += s.live[p + d] > mine[u] ? 1u : 0u;
+          const unsigned long long* b = s.live + st;
+          for (uint32_t e = 0; e < cnt; ++e) {
+            const unsigned long long o = b[e];
+            r += (o > lkey[u] || (o == lkey[u] && e < slot)) ? 1u : 0u;
           }
-          fin = st + r;
         }
+        const uint32_t fin = st + r;
         if (fin < (uint32_t)ksel) {
-          os[fin] = __uint_as_float(score_bits((uint32_t)(mine[u] >> 32)));
-          oi[fin] = src.out_id_from(rbase, (uint32_t)mine[u]);
-        }
-      }
-      const int nbig = min((int)s.nbig, kBigMax);
-      for (int i = tid; i < nbig; i += NT) {
-        const uint32_t ent = s.big[i];
-        const uint32_t st = ent >> 8, cnt = ent & 0xFFu;
-        const uint32_t nout = min(cnt, (uint32_t)ksel - st);
-        if (cnt <= 8u) {
-          unsigned long long a[8];
-          sort8_desc(s.live + st, cnt, a);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if ((uint32_t)j < nout) {
-              os[st + j] = __uint_as_float(score_bits((uint32_t)(a[j] >> 32)));
-              oi[st + j] = src.out_id_from(rbase, (uint32_t)a[j]);
-            }
-          }
-        } else {
-          for (uint32_t m = 0; m < cnt; ++m) {
-            const unsigned long long mine = s.live[st + m];
-            uint32_t r = 0u;
-            for (uint32_t e = 0; e < cnt; ++e) {
-              const unsigned long long o = s.live[st + e];
-              r += (o > mine || (e < m && o == mine)) ? 1u : 0u;
-            }
-            if (r < nout) {
-              os[st + r] = __uint_as_float(score_bits((uint32_t)(mine >> 32)));
-              oi[st + r] = src.out_id_from(rbase, (uint32_t)mine);
-            }
-          }
+          ostage[fin] = score_bits((uint32_t)(lkey[u] >> 32));
+          ostage[K + fin] = (uint32_t)src.out_id_from(rbase, (uint32_t)lkey[u]);
         }
       }
       for (int j = ksel + tid; j < K; j += NT) {
-        os[j] = __uint_as_float(0xFF800000u);
-        oi[j] = -1;
+        ostage[j] = 0xFF800000u;  // -inf
+        ostage[K + j] = 0xFFFFFFFFu;  // -1
       }
     } else {
       // ---- Fallback: radix select + sort, reading the row from global memory -
@@ -636,11 +559,32 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     }
     __syncthreads();  // every reader of this row's shared state is done
 
-    zero_words<NT>(s.u.table, kHistBins);
-    zero_words<NT>(s.fine, kFineMax);
+    // Write the staged output (16-byte stores where K and the output rows
+    // allow), zeroing `fine` and the table behind it: each thread zeroes only
+    // the words it copied, so no barrier is needed between the two.
+    constexpr int kRegion = kFineMax + kHistBins;  // fine, then the table
+    const bool vec_out =
+        (K & 3) == 0 && ((reinterpret_cast<uintptr_t>(os) | reinterpret_cast<uintptr_t>(oi)) & 15u) == 0u;
+    if (fast && !vec_out) {
+      for (int j = tid; j < K; j += NT) {
+        os[j] = __uint_as_float(ostage[j]);
+        oi[j] = (int32_t)ostage[K + j];
+      }
+      __syncthreads();
+    }
+    for (int i = 4 * tid; i < kRegion; i += 4 * NT) {
+      uint4* w = reinterpret_cast<uint4*>(s.fine + i);
+      if (fast && vec_out && i < 2 * K) {
+        const uint4 v = *w;
+        if (i < K)
+          *reinterpret_cast<uint4*>(os + i) = v;
+        else
+          *reinterpret_cast<uint4*>(oi + (i - K)) = v;
+      }
+      *w = make_uint4(0u, 0u, 0u, 0u);
+    }
     if (tid == 0) {
       s.live_cursor = 0u;
-      s.nbig = 0u;
       s.overflow = 0u;
       s.stat_or[0] = s.stat_or[1] = 0u;
       s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
