@@ -368,13 +368,17 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
 
     // ---- COMPACT: live candidates into a dense list -------------------------
     if (fast) {
-      uint32_t mask = 0u, cnt = 0u;
+      uint32_t mask = 0u;
+      const uint32_t lf = live_from << 10;  // live: key >= lf
+      if (lf != 0u) {
+        // candidates past the row hold key 0 (< lf)
 #pragma unroll
-      for (int j = 0; j < kItems; ++j) {
-        const bool lv = (tid + (j >> 2) * NT) < n4 && (keys[j] >> 10) >= live_from;
-        mask |= (lv ? 1u : 0u) << j;
-        cnt += lv ? 1u : 0u;
+        for (int j = 0; j < kItems; ++j) mask |= (keys[j] >= lf ? 1u : 0u) << j;
+      } else {
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) mask |= ((tid + (j >> 2) * NT) < n4 ? 1u : 0u) << j;
       }
+      const uint32_t cnt = __popc(mask);
       const uint32_t incl = warp_inclusive_scan(cnt);
       uint32_t base = 0u;
       if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
@@ -385,7 +389,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       uint32_t ior = 0u, iand = 0xFFFFFFFFu;
 #pragma unroll
       for (int v = 0; v < kVec; ++v) {
-        if ((mask >> (4 * v)) & 0xFu) {
+        if ((tid + v * NT) < n4) {
           const uint4 u4 = src.inv4(stage, tid + v * NT);
           const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
@@ -498,6 +502,10 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       // ---- SCATTER: members of shared buckets starting before K ------------
       // gslot[u] becomes the bucket's start << 16 | size << 8 | this key's
       // slot in it (kNone for a key whose bucket starts at or after K).
+      // Members of one bucket share their key's top 11 bits (the L1 bin), so
+      // the list holds rank_key(key, slot) = key << 11 | (255 - slot): the
+      // key order within the bucket, identical keys told apart by their slot
+      // (the smaller slot ranks first).
 #pragma unroll
       for (int u = 0; u < kLivePer; ++u) {
         if (gslot[u] != kNone) {
@@ -505,28 +513,31 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
           gslot[u] = kNone;
           if ((old >> 16) < (uint32_t)ksel) {
             gslot[u] = old;
-            if (((old >> 8) & 0xFFu) > 1u) s.live[(old >> 16) + (old & 0xFFu)] = lkey[u];
+            if (((old >> 8) & 0xFFu) > 1u)
+              s.live[(old >> 16) + (old & 0xFFu)] = (lkey[u] << 11) | (255u - (old & 0xFFu));
           }
         }
       }
       __syncthreads();
 
       // ---- RANK: position = bucket start + members ranking above ----------
-      // A member ranks above another when its key is larger, or equal with
-      // a smaller slot (identical keys are interchangeable).
       const uint32_t rbase = src.row_base(t);
 #pragma unroll
       for (int u = 0; u < kLivePer; ++u) {
         const uint32_t en = gslot[u];
         if (en == kNone) continue;
         const uint32_t st = en >> 16, cnt = (en >> 8) & 0xFFu, slot = en & 0xFFu;
+        const unsigned long long* b = s.live + st;
+        const unsigned long long mine = (lkey[u] << 11) | (255u - slot);
         uint32_t r = 0u;
-        if (cnt > 1u) {
-          const unsigned long long* b = s.live + st;
-          for (uint32_t e = 0; e < cnt; ++e) {
-            const unsigned long long o = b[e];
-            r += (o > lkey[u] || (o == lkey[u] && e < slot)) ? 1u : 0u;
-          }
+        if (__all_sync(__activemask(), cnt <= 8u)) {
+          // buckets of up to 8: a fixed window, no loop (a single key
+          // compares with itself as not larger)
+#pragma unroll
+          for (uint32_t e = 0; e < 8u; ++e)
+            if (e < cnt && cnt > 1u) r += b[e] > mine ? 1u : 0u;
+        } else if (cnt > 1u) {
+          for (uint32_t e = 0; e < cnt; ++e) r += b[e] > mine ? 1u : 0u;
         }
         const uint32_t fin = st + r;
         if (fin < (uint32_t)ksel) {
