@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   p += align16((size_t)n * 4);
   uint32_t* sinv = reinterpret_cast<uint32_t*>(p);
 
+  grid_dependency_wait();
   const int grid = (int)gridDim.x;
   const int b = (int)blockIdx.x;
   for (int cs = 0; cs < T; cs += kChunkRows) {
@@ -393,6 +394,26 @@ static cudaError_t device_info(DeviceInfo** out) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Launches with programmatic stream serialization: the grid may be scheduled
+// while the stream's previous kernel is still finishing, and waits for it
+// (griddepcontrol.wait, first thing in every kernel here) before touching
+// memory.  Only the launch latency overlaps; the ordering is the stream's.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_serialized(void (*kernel)(KArgs...), int grid, int block, size_t smem,
+                                     cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // A kernel whose row copy is armed but never issued: exercises the bounded
 // wait and the status report.
 __global__ void wait_timeout_selftest_kernel(unsigned long long limit, unsigned int* status) {
@@ -420,28 +441,29 @@ static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out
   const size_t smem = stream_smem_bytes(words);
   const bool stream_ok =
       src.vec4 && K <= kStreamMaxK && smem <= (size_t)d->max_smem_optin && n <= kStreamMaxNWide;
+  cudaError_t e;
   if (stream_ok && n > kStreamMaxN) {
     // up to 16384 candidates per row: one 1024-thread CTA per SM
-    unsigned int* status = d->status;
     const int grid = T < d->sms ? T : d->sms;
-    topk_stream_kernel<1024, kStreamMaxNWide, Source>
-        <<<grid, 1024, smem, stream>>>(src, T, K, out_scores, out_ids, status);
+    e = launch_serialized(topk_stream_kernel<1024, kStreamMaxNWide, Source>, grid, 1024, smem,
+                          stream, src, T, K, out_scores, out_ids, d->status);
   } else if (stream_ok) {
-    unsigned int* status = d->status;
     if (T <= d->sms) {
-      topk_stream_kernel<1024, kStreamMaxN, Source>
-          <<<T, 1024, smem, stream>>>(src, T, K, out_scores, out_ids, status);
+      e = launch_serialized(topk_stream_kernel<1024, kStreamMaxN, Source>, T, 1024, smem, stream,
+                            src, T, K, out_scores, out_ids, d->status);
     } else {
       const int grid = T < 2 * d->sms ? T : 2 * d->sms;
-      topk_stream_kernel<512, kStreamMaxN, Source>
-          <<<grid, 512, smem, stream>>>(src, T, K, out_scores, out_ids, status);
+      e = launch_serialized(topk_stream_kernel<512, kStreamMaxN, Source>, grid, 512, smem, stream,
+                            src, T, K, out_scores, out_ids, d->status);
     }
   } else {
     const size_t gsmem = row_smem_bytes(n, K);
     if (gsmem > (size_t)d->max_smem_optin) return DCP_ERR_UNSUPPORTED;
     const int grid = T < d->sms ? T : d->sms;
-    topk_rows_kernel<Source><<<grid, kThreads, gsmem, stream>>>(src, T, K, out_scores, out_ids);
+    e = launch_serialized(topk_rows_kernel<Source>, grid, kThreads, gsmem, stream, src, T, K,
+                          out_scores, out_ids);
   }
+  if (e != cudaSuccess) return DCP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
 }
 

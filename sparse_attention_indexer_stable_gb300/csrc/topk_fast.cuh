@@ -137,6 +137,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint3
   return false;
 }
 
+// Programmatic dependent launch: wait until the stream's previous grid has
+// completed and its memory is visible (a no-op when the launch did not allow
+// overlap), then let the next grid be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* gmem, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(gmem), "r"(bytes) : "memory");
@@ -238,6 +246,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
 
+  grid_dependency_wait();
   zero_words<NT>(s.fine, kFineMax + kHistBins);  // fine and the table behind it
   if (tid == 0) {
     s.live_cursor = 0u;
