@@ -51,12 +51,17 @@ struct SelectShared {
   uint32_t dup_claim;
 };
 
+// Inclusive prefix sum across the warp (all 32 lanes active).  The shuffle's
+// predicate says whether the source lane exists, so each step is a shuffle
+// and a predicated add.
 __device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v) {
-  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t u = __shfl_up_sync(0xFFFFFFFFu, v, o);
-    if (lane >= o) v += u;
+    asm("{\n .reg .u32 t;\n .reg .pred p;\n"
+        " shfl.sync.up.b32 t|p, %0, %1, 0, 0xffffffff;\n"
+        " @p add.u32 %0, %0, t;\n}\n"
+        : "+r"(v)
+        : "r"(o));
   }
   return v;
 }

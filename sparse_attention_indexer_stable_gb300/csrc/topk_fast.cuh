@@ -313,36 +313,46 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     __syncthreads();
 
     // ---- SCAN1: bins high to low; packed (buckets << 16 | candidates) -------
+    // A warp whose bins are all empty (most warps: the keys fill a narrow
+    // band of bins) only reports a zero total.
     {
       uint32_t h[kBinsPer], f[kBinsPer];
       load_bins_desc<kBinsPer>(s.u.table + kHistBins - kBinsPer * (tid + 1), h);
-      uint32_t local = 0u;
+      uint32_t any = 0u;
 #pragma unroll
-      for (int e = 0; e < kBinsPer; ++e) {
-        f[e] = fine_buckets(h[e]);
-        local += (f[e] << 16) | h[e];
+      for (int e = 0; e < kBinsPer; ++e) any |= h[e];
+      const bool warp_busy = __any_sync(0xFFFFFFFFu, any != 0u);
+      uint32_t local = 0u, incl = 0u;
+      if (warp_busy) {
+#pragma unroll
+        for (int e = 0; e < kBinsPer; ++e) {
+          f[e] = fine_buckets(h[e]);
+          local += (f[e] << 16) | h[e];
+        }
+        incl = warp_inclusive_scan(local);
       }
-      const uint32_t incl = warp_inclusive_scan(local);
       if (lane == 31) s.wa[warp] = incl;
       __syncthreads();
-      // every warp scans the per-warp totals itself (no second barrier)
-      const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
-      const uint32_t wti = warp_inclusive_scan(wt);
-      uint32_t ex = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
+      if (warp_busy) {
+        // every warp scans the per-warp totals itself (no second barrier)
+        const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
+        const uint32_t wti = warp_inclusive_scan(wt);
+        uint32_t ex = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
 #pragma unroll
-      for (int e = 0; e < kBinsPer; ++e) {
-        const uint32_t above = ex & 0xFFFFu, fabove = ex >> 16;
-        const int b = kHistBins - 1 - (kBinsPer * tid + e);
-        if (h[e] != 0u) {
-          if (above < (uint32_t)ksel && (uint32_t)ksel <= above + h[e]) {
-            s.b1 = (uint32_t)b;
-            s.nlive = above + h[e];
-            s.nfine = fabove + f[e];
-            s.above_b1 = above;
+        for (int e = 0; e < kBinsPer; ++e) {
+          const uint32_t above = ex & 0xFFFFu, fabove = ex >> 16;
+          const int b = kHistBins - 1 - (kBinsPer * tid + e);
+          if (h[e] != 0u) {
+            if (above < (uint32_t)ksel && (uint32_t)ksel <= above + h[e]) {
+              s.b1 = (uint32_t)b;
+              s.nlive = above + h[e];
+              s.nfine = fabove + f[e];
+              s.above_b1 = above;
+            }
+            s.u.table[b] = (fabove << 8) | (uint32_t)(31 - __clz(f[e]));
           }
-          s.u.table[b] = (fabove << 8) | (uint32_t)(31 - __clz(f[e]));
+          ex += (f[e] << 16) | h[e];
         }
-        ex += (f[e] << 16) | h[e];
       }
     }
     __syncthreads();
@@ -472,32 +482,38 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     // fine[g] becomes start << 16 | min(size, 255) << 8, its low byte the
     // fill cursor for SCATTER.
     if (fast) {
+      // warps whose buckets all lie past the last one only report a zero total
+      const bool warp_busy = kFinePer * 32 * warp < nfine;
       uint32_t c[kFinePer];
-      uint32_t local = 0u;
+      uint32_t local = 0u, incl = 0u;
+      if (warp_busy) {
 #pragma unroll
-      for (int e = 0; e < kFinePer; ++e) {
-        const int g = kFinePer * tid + e;
-        c[e] = g < nfine ? s.fine[g] : 0u;
-        local += c[e];
+        for (int e = 0; e < kFinePer; ++e) {
+          const int g = kFinePer * tid + e;
+          c[e] = g < nfine ? s.fine[g] : 0u;
+          local += c[e];
+        }
+        incl = warp_inclusive_scan(local);
       }
-      const uint32_t incl = warp_inclusive_scan(local);
       if (lane == 31) s.wa[warp] = incl;
       __syncthreads();
-      const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
-      const uint32_t wti = warp_inclusive_scan(wt);
-      uint32_t st = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
-      uint32_t over = 0u;
+      if (warp_busy) {
+        const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
+        const uint32_t wti = warp_inclusive_scan(wt);
+        uint32_t st = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
+        uint32_t over = 0u;
 #pragma unroll
-      for (int e = 0; e < kFinePer; ++e) {
-        const int g = kFinePer * tid + e;
-        if (g < nfine) {
-          s.fine[g] = (st << 16) | (min(c[e], 255u) << 8);
-          if (st < (uint32_t)ksel && c[e] > kBigBucket) over = 1u;
-          st += c[e];
+        for (int e = 0; e < kFinePer; ++e) {
+          const int g = kFinePer * tid + e;
+          if (g < nfine) {
+            s.fine[g] = (st << 16) | (min(c[e], 255u) << 8);
+            if (st < (uint32_t)ksel && c[e] > kBigBucket) over = 1u;
+            st += c[e];
+          }
         }
+        over = __reduce_or_sync(0xFFFFFFFFu, over);
+        if (lane == 0 && over) s.overflow = 1u;
       }
-      over = __reduce_or_sync(0xFFFFFFFFu, over);
-      if (lane == 0 && over) s.overflow = 1u;
     }
     __syncthreads();
     fast = fast && s.overflow == 0u;

@@ -182,6 +182,32 @@ def test_stream_and_graph_replay():
                 "replay")
 
 
+def test_stream_order_around_serialized_launches():
+    """Kernels are launched so that they may be scheduled while the stream's
+    previous kernel finishes; each must still see the inputs a preceding
+    torch kernel writes, and a following torch kernel must see its outputs.
+    Back-to-back iterations on one stream, no host sync in between."""
+    ms = [workloads.decode(seed=40 + j) if j % 2 == 0 else workloads.tieheavy(seed=40 + j)
+          for j in range(6)]
+    neg_s = [_dev(-m.scores) for m in ms]
+    ids = [_dev(m.ids) for m in ms]
+    s = torch.empty_like(neg_s[0])
+    i = torch.empty_like(ids[0])
+    out_ids = torch.empty((ms[0].T, ms[0].K), dtype=torch.int32, device="cuda")
+    out_scores = torch.empty((ms[0].T, ms[0].K), dtype=torch.float32, device="cuda")
+    got_ids, got_scores = [], []
+    for j in range(len(ms)):
+        torch.neg(neg_s[j], out=s)           # a kernel writes the scores
+        torch.add(ids[j], 0, out=i)          # and the ids
+        dk.merge(s, i, out_ids=out_ids, out_scores=out_scores)
+        got_ids.append(out_ids + 0)          # kernels read the outputs
+        got_scores.append(out_scores * 1.0)
+    torch.cuda.synchronize()
+    for j, m in enumerate(ms):
+        assert_same((got_ids[j].cpu().numpy(), got_scores[j].cpu().numpy()),
+                    oracle.merge(m.scores, m.ids), f"iteration {j}")
+
+
 # --------------------------------------------------------------- local top-K
 def run_local(logits, K, rank, dcp, L=None, row_starts=None):
     x = _dev(logits)
