@@ -56,30 +56,34 @@ struct MergeSource {
     }
   }
 
-  // Fast path staging: the row's scores, then its ids, as 16-byte copies
-  // straight from the rank-major layout (needs K % 4 == 0 and 16-byte
-  // aligned bases).
-  __host__ __device__ int staged_words() const { return 2 * dcp * K; }
+  // Fast path staging: the row's scores and its ids, each as dcp 16-byte
+  // copies straight from the rank-major layout (needs K % 4 == 0 and
+  // 16-byte aligned bases), completing on separate barriers.
+  static constexpr bool kStagesIds = true;
+  __host__ __device__ int score_words() const { return dcp * K; }
+  __host__ __device__ int ids_words() const { return dcp * K; }
 
-  // One thread: arm `bar` with the row's bytes and copy row t's scores then
-  // ids into dst (needs K % 4 == 0 and 16-byte aligned bases).
-  __device__ void issue_tma(int t, uint32_t* dst, unsigned long long* bar) const {
+  // One thread: arm `bar` with the bytes of row t's scores and copy them to dst.
+  __device__ void issue_scores(int t, uint32_t* dst, unsigned long long* bar) const {
     const uint32_t seg = (uint32_t)K * 4u;
-    mbar_expect_tx(bar, 2u * (uint32_t)dcp * seg);
+    mbar_expect_tx(bar, (uint32_t)dcp * seg);
     const size_t stride = (size_t)T * (size_t)K;
     const float* sp = scores + (size_t)t * (size_t)K;
-    const int32_t* ip = ids + (size_t)t * (size_t)K;
-    for (int r = 0; r < dcp; ++r, sp += stride, ip += stride) {
-      tma_load_1d(dst + r * K, sp, seg, bar);
-      tma_load_1d(dst + dcp * K + r * K, ip, seg, bar);
-    }
+    for (int r = 0; r < dcp; ++r, sp += stride) tma_load_1d(dst + r * K, sp, seg, bar);
   }
 
-  __device__ uint32_t inv(const uint32_t* buf, int i) const { return ~buf[dcp * K + i]; }
+  // One thread: the same for row t's ids.
+  __device__ void issue_ids(int t, uint32_t* dst, unsigned long long* bar) const {
+    const uint32_t seg = (uint32_t)K * 4u;
+    mbar_expect_tx(bar, (uint32_t)dcp * seg);
+    const size_t stride = (size_t)T * (size_t)K;
+    const int32_t* ip = ids + (size_t)t * (size_t)K;
+    for (int r = 0; r < dcp; ++r, ip += stride) tma_load_1d(dst + r * K, ip, seg, bar);
+  }
 
-  // Inverted ids of staged candidates 4c .. 4c+3.
-  __device__ uint4 inv4(const uint32_t* buf, int c) const {
-    const uint4 w = *reinterpret_cast<const uint4*>(buf + dcp * K + 4 * c);
+  // Inverted ids of staged candidates 4c .. 4c+3 (staged ids at `staged`).
+  __device__ uint4 inv4(const uint32_t* staged, int c) const {
+    const uint4 w = *reinterpret_cast<const uint4*>(staged + 4 * c);
     return make_uint4(~w.x, ~w.y, ~w.z, ~w.w);
   }
 
@@ -149,14 +153,16 @@ struct LocalSource {
     }
   }
 
-  __host__ __device__ int staged_words() const { return L; }
+  // Ids are column numbers: only the logits are staged.
+  static constexpr bool kStagesIds = false;
+  __host__ __device__ int score_words() const { return L; }
+  __host__ __device__ int ids_words() const { return 0; }
 
-  __device__ void issue_tma(int t, uint32_t* dst, unsigned long long* bar) const {
+  __device__ void issue_scores(int t, uint32_t* dst, unsigned long long* bar) const {
     mbar_expect_tx(bar, (uint32_t)L * 4u);
     tma_load_1d(dst, logits + (size_t)t * (size_t)ld, (uint32_t)L * 4u, bar);
   }
-
-  __device__ uint32_t inv(const uint32_t*, int i) const { return ~(uint32_t)i; }
+  __device__ void issue_ids(int, uint32_t*, unsigned long long*) const {}
 
   __device__ uint4 inv4(const uint32_t*, int c) const {
     const uint32_t i = 4u * (uint32_t)c;
@@ -214,15 +220,17 @@ struct FusedSource {
     }
   }
 
-  __host__ __device__ int staged_words() const { return dcp * L; }
+  // Ids are r*L + c: only the logits are staged.
+  static constexpr bool kStagesIds = false;
+  __host__ __device__ int score_words() const { return dcp * L; }
+  __host__ __device__ int ids_words() const { return 0; }
 
-  __device__ void issue_tma(int t, uint32_t* dst, unsigned long long* bar) const {
+  __device__ void issue_scores(int t, uint32_t* dst, unsigned long long* bar) const {
     const uint32_t seg = (uint32_t)L * 4u;
     mbar_expect_tx(bar, (uint32_t)dcp * seg);
     for (int r = 0; r < dcp; ++r) tma_load_1d(dst + r * L, row(t, r), seg, bar);
   }
-
-  __device__ uint32_t inv(const uint32_t*, int i) const { return ~(uint32_t)i; }
+  __device__ void issue_ids(int, uint32_t*, unsigned long long*) const {}
 
   __device__ uint4 inv4(const uint32_t*, int c) const {
     const uint32_t i = 4u * (uint32_t)c;
@@ -437,8 +445,7 @@ static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out
                               int32_t* out_ids, cudaStream_t stream) {
   DeviceInfo* d = nullptr;
   if (device_info(&d) != cudaSuccess) return DCP_ERR_CUDA;
-  const int words = src.staged_words();
-  const size_t smem = stream_smem_bytes(words);
+  const size_t smem = stream_smem_bytes(src.score_words(), src.ids_words());
   const bool stream_ok =
       src.vec4 && K <= kStreamMaxK && smem <= (size_t)d->max_smem_optin && n <= kStreamMaxNWide;
   cudaError_t e;

@@ -53,6 +53,7 @@ constexpr int kStreamMaxK = 2048;
 constexpr int kLiveMax = 3072;                // live candidates per row
 constexpr int kFineMax = kStreamMaxK + 1024;  // fine buckets per row (bound, see SCAN1)
 constexpr uint32_t kBigBucket = 255;          // a larger bucket starting before K sends the row to the fallback
+constexpr int kRankMax = kStreamMaxK + 256;   // list positions up to the end of the bucket straddling K
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr unsigned long long kStageWaitLimit = 1ull << 31;  // cycles (about 1 s) to wait for a row's copy
 constexpr uint32_t kStatusCopyTimeout = 1u;     // device status bit: a staging copy timed out
@@ -74,8 +75,10 @@ struct StreamShared {
   uint32_t nfine;                     // fine buckets of bins >= b1
   uint32_t above_b1;                  // candidates in bins above b1
   uint32_t found_digit, found_above, found_count;  // refinement of b1
+  uint32_t p_end;                     // end of the bucket straddling K
   uint32_t overflow;                  // a bucket to rank is too large
-  unsigned long long stage_bar;       // completes when a row's copies into the stage land
+  unsigned long long stage_bar;       // completes when a row's scores land in the stage
+  unsigned long long ids_bar;         // completes when a row's ids land in the aux region
 };
 // 16-byte vector accesses to these arrays need 16-byte aligned offsets.
 static_assert(offsetof(StreamShared, live) % 16 == 0, "live must be 16-byte aligned");
@@ -83,6 +86,10 @@ static_assert(offsetof(StreamShared, fine) % 16 == 0, "fine must be 16-byte alig
 static_assert(offsetof(StreamShared, u) == offsetof(StreamShared, fine) + sizeof(uint32_t) * kFineMax,
               "the table must follow fine directly (one region for output staging and reset)");
 static_assert(2 * kStreamMaxK <= kFineMax + kHistBins, "output staging must fit fine + table");
+static_assert(kRankMax >= kStreamMaxK + (int)kBigBucket - 1, "list positions must reach the straddling bucket's end");
+// Scratch for RANK in the aux region: rank keys (u64) then bucket info (u16)
+// per list position.
+constexpr int kScratchWords = (kRankMax * 8 + kRankMax * 2 + 15) / 16 * 4;
 static_assert(offsetof(StreamShared, stage_bar) % 8 == 0, "mbarrier must be 8-byte aligned");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -213,9 +220,19 @@ __device__ __forceinline__ void find_digit_desc(const uint32_t* hist, uint32_t n
   }
 }
 
-// Shared-memory bytes of the streaming kernel for a row staging `words` words.
-inline size_t stream_smem_bytes(int words) {
-  return ((sizeof(StreamShared) + 15) & ~(size_t)15) + (size_t)((words + 3) & ~3) * 4;
+// Shared-memory bytes of the streaming kernel: the state, the stage for a
+// row's `score_words` scores, and the aux region (the row's `ids_words` ids
+// when they are staged, RANK's scratch after COMPACT; the larger of the two).
+inline size_t stream_smem_bytes(int score_words, int ids_words) {
+  const int aux = ids_words > kScratchWords ? ids_words : kScratchWords;
+  return ((sizeof(StreamShared) + 15) & ~(size_t)15) + (size_t)((score_words + 3) & ~3) * 4 +
+         (size_t)((aux + 3) & ~3) * 4;
+}
+
+// Orders this thread's earlier shared-memory writes before later bulk copies
+// (async proxy) into the same memory.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
 // Zeroes `words` (a multiple of 4) 16-byte-aligned shared words.
@@ -241,6 +258,9 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   uint32_t* stage =
       reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(StreamShared) + 15) & ~(size_t)15));
   const int n = src.count();  // multiple of 4, <= MAXN
+  uint32_t* aux = stage + n;  // the row's ids (when staged), then RANK's scratch
+  unsigned long long* rkl = reinterpret_cast<unsigned long long*>(aux);
+  uint16_t* info = reinterpret_cast<uint16_t*>(rkl + kRankMax);
   const int n4 = n >> 2;
   const int ksel = K < n ? K : n;
   const int tid = threadIdx.x;
@@ -250,6 +270,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   zero_words<NT>(s.fine, kFineMax + kHistBins);  // fine and the table behind it
   if (tid == 0) {
     s.live_cursor = 0u;
+    s.p_end = 0u;
     s.overflow = 0u;
     s.stat_or[0] = s.stat_or[1] = 0u;
     s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
@@ -262,11 +283,15 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   int t = (int)blockIdx.x;
   if (tid == 0) {
     mbar_init(&s.stage_bar, 1u);
+    mbar_init(&s.ids_bar, 1u);
     mbar_fence_init();
   }
   __syncthreads();
   if (tid == 0) {
-    if (t < T) src.issue_tma(t, stage, &s.stage_bar);
+    if (t < T) {
+      src.issue_scores(t, stage, &s.stage_bar);
+      if constexpr (Source::kStagesIds) src.issue_ids(t, aux, &s.ids_bar);
+    }
     if (t + G < T) src.prefetch_l2(t + G);
   }
 
@@ -274,15 +299,17 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     const bool staged = mbar_wait_bounded(&s.stage_bar, k & 1u, kStageWaitLimit);
     // the row is staged (or its copy timed out) and the previous row's state reset
     if (__syncthreads_or(!staged)) {
-      // Report the timeout and stop this CTA; first give the copy a last,
+      // Report the timeout and stop this CTA; first give the copies a last,
       // bounded chance to land so no copy is left writing into shared memory.
       if (tid == 0) atomicOr(status, kStatusCopyTimeout);
       mbar_wait_bounded(&s.stage_bar, k & 1u, kStageWaitLimit);
+      if constexpr (Source::kStagesIds) mbar_wait_bounded(&s.ids_bar, k & 1u, kStageWaitLimit);
       return;
     }
-    // Rows stream from HBM into L2 two rows ahead of their use; the copy of
-    // the next row into shared memory starts as soon as this row's staged
-    // data is consumed (after COMPACT).
+    // Rows stream from HBM into L2 two rows ahead of their use.  The copy of
+    // the next row's scores into the stage starts as soon as this row's are
+    // consumed (after COMPACT); its ids follow at the end of the row (the
+    // aux region serves RANK until then) and are needed only by COMPACT.
     if (tid == 0 && t + 2 * G < T) src.prefetch_l2(t + 2 * G);
 
     // ---- L1: histogram of the score keys' top 11 bits ---------------------
@@ -355,7 +382,17 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         }
       }
     }
-    __syncthreads();
+    if constexpr (Source::kStagesIds) {
+      // COMPACT reads the row's ids: they were copied during L1 and SCAN1
+      const bool ids_ok = mbar_wait_bounded(&s.ids_bar, k & 1u, kStageWaitLimit);
+      if (__syncthreads_or(!ids_ok)) {
+        if (tid == 0) atomicOr(status, kStatusCopyTimeout);
+        mbar_wait_bounded(&s.ids_bar, k & 1u, kStageWaitLimit);
+        return;
+      }
+    } else {
+      __syncthreads();
+    }
 
     const uint32_t b1 = s.b1;
     const int nfine = (int)s.nfine;
@@ -409,7 +446,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
 #pragma unroll
       for (int v = 0; v < kVec; ++v) {
         if ((tid + v * NT) < n4) {
-          const uint4 u4 = src.inv4(stage, tid + v * NT);
+          const uint4 u4 = src.inv4(aux, tid + v * NT);
           const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -430,7 +467,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     __syncthreads();
     // The staged row is consumed (the fallback re-reads its row from global
     // memory): stream the next row in behind the rest of this one.
-    if (tid == 0 && t + G < T) src.issue_tma(t + G, stage, &s.stage_bar);
+    if (tid == 0 && t + G < T) src.issue_scores(t + G, stage, &s.stage_bar);
 
     // ---- L2: fine bucket of every live candidate ---------------------------
     unsigned long long lkey[kLivePer];
@@ -507,7 +544,10 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
           const int g = kFinePer * tid + e;
           if (g < nfine) {
             s.fine[g] = (st << 16) | (min(c[e], 255u) << 8);
-            if (st < (uint32_t)ksel && c[e] > kBigBucket) over = 1u;
+            if (st < (uint32_t)ksel) {
+              if (c[e] > kBigBucket) over = 1u;
+              if ((uint32_t)ksel <= st + c[e]) s.p_end = st + c[e];
+            }
             st += c[e];
           }
         }
@@ -524,50 +564,58 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     // row's scores in words [0, K), its ids in [K, 2K).
     uint32_t* ostage = s.fine;
     if (fast) {
-      // ---- SCATTER: members of shared buckets starting before K ------------
-      // gslot[u] becomes the bucket's start << 16 | size << 8 | this key's
-      // slot in it (kNone for a key whose bucket starts at or after K).
-      // Members of one bucket share their key's top 11 bits (the L1 bin), so
-      // the list holds rank_key(key, slot) = key << 11 | (255 - slot): the
-      // key order within the bucket, identical keys told apart by their slot
-      // (the smaller slot ranks first).
+      // ---- SCATTER: winners' keys into the list, in bucket order -----------
+      // Members of buckets that start before K go to their bucket's slots.
+      // Per list position the aux region records the bucket's size << 8 | the
+      // slot and, for shared buckets, rank_key(key, slot) =
+      // key << 11 | (255 - slot): members of a bucket share their key's top
+      // 11 bits (the L1 bin), so this is the key order within the bucket,
+      // identical keys told apart by their slot (the smaller slot first).
 #pragma unroll
       for (int u = 0; u < kLivePer; ++u) {
         if (gslot[u] != kNone) {
           const uint32_t old = atomicAdd(&s.fine[gslot[u]], 1u);
-          gslot[u] = kNone;
           if ((old >> 16) < (uint32_t)ksel) {
-            gslot[u] = old;
-            if (((old >> 8) & 0xFFu) > 1u)
-              s.live[(old >> 16) + (old & 0xFFu)] = (lkey[u] << 11) | (255u - (old & 0xFFu));
+            const uint32_t pos = (old >> 16) + (old & 0xFFu);
+            s.live[pos] = lkey[u];
+            info[pos] = (uint16_t)(old & 0xFFFFu);
+            if (((old >> 8) & 0xFFu) > 1u) rkl[pos] = (lkey[u] << 11) | (255u - (old & 0xFFu));
           }
         }
       }
       __syncthreads();
 
       // ---- RANK: position = bucket start + members ranking above ----------
+      // Per list position.  Consecutive positions share buckets, so a warp's
+      // buckets are usually all small enough for a 4-wide window.
+      const uint32_t p_end = min(s.p_end, (uint32_t)kRankMax);
       const uint32_t rbase = src.row_base(t);
-#pragma unroll
-      for (int u = 0; u < kLivePer; ++u) {
-        const uint32_t en = gslot[u];
-        if (en == kNone) continue;
-        const uint32_t st = en >> 16, cnt = (en >> 8) & 0xFFu, slot = en & 0xFFu;
-        const unsigned long long* b = s.live + st;
-        const unsigned long long mine = (lkey[u] << 11) | (255u - slot);
+      for (uint32_t p = tid; p < p_end; p += NT) {
+        const uint32_t inf = info[p];
+        const uint32_t cnt = inf >> 8;
+        const uint32_t st = p - (inf & 0xFFu);
+        const unsigned long long key = s.live[p];
+        const uint32_t mc = __reduce_max_sync(__activemask(), cnt);
         uint32_t r = 0u;
-        if (__all_sync(__activemask(), cnt <= 8u)) {
-          // buckets of up to 8: a fixed window, no loop (a single key
-          // compares with itself as not larger)
+        if (mc > 1u) {
+          const unsigned long long* b = rkl + st;
+          const unsigned long long mine = rkl[p];
+          if (mc <= 4u) {
 #pragma unroll
-          for (uint32_t e = 0; e < 8u; ++e)
-            if (e < cnt && cnt > 1u) r += b[e] > mine ? 1u : 0u;
-        } else if (cnt > 1u) {
-          for (uint32_t e = 0; e < cnt; ++e) r += b[e] > mine ? 1u : 0u;
+            for (uint32_t e = 0; e < 4u; ++e)
+              if (e < cnt && cnt > 1u) r += b[e] > mine ? 1u : 0u;
+          } else if (mc <= 8u) {
+#pragma unroll
+            for (uint32_t e = 0; e < 8u; ++e)
+              if (e < cnt && cnt > 1u) r += b[e] > mine ? 1u : 0u;
+          } else if (cnt > 1u) {
+            for (uint32_t e = 0; e < cnt; ++e) r += b[e] > mine ? 1u : 0u;
+          }
         }
         const uint32_t fin = st + r;
         if (fin < (uint32_t)ksel) {
-          ostage[fin] = score_bits((uint32_t)(lkey[u] >> 32));
-          ostage[K + fin] = (uint32_t)src.out_id_from(rbase, (uint32_t)lkey[u]);
+          ostage[fin] = score_bits((uint32_t)(key >> 32));
+          ostage[K + fin] = (uint32_t)src.out_id_from(rbase, (uint32_t)key);
         }
       }
       for (int j = ksel + tid; j < K; j += NT) {
@@ -593,7 +641,12 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         }
       }
     }
+    // RANK wrote the aux region through ordinary stores; the next row's ids
+    // are copied into it after the barrier.
+    if constexpr (Source::kStagesIds) fence_proxy_async_shared();
     __syncthreads();  // every reader of this row's shared state is done
+    if constexpr (Source::kStagesIds)
+      if (tid == 0 && t + G < T) src.issue_ids(t + G, aux, &s.ids_bar);
 
     // Write the staged output (16-byte stores where K and the output rows
     // allow), zeroing `fine` and the table behind it: each thread zeroes only
@@ -621,6 +674,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     }
     if (tid == 0) {
       s.live_cursor = 0u;
+      s.p_end = 0u;
       s.overflow = 0u;
       s.stat_or[0] = s.stat_or[1] = 0u;
       s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
