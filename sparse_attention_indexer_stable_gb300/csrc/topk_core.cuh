@@ -31,13 +31,14 @@ constexpr int kHistBins = 2048;
 
 // Order-preserving map of fp32 bits to u32: unsigned order of the result is
 // float order, with -0.0 just below +0.0 and NaNs outside the finite range.
+// Negative values have every bit inverted, the others only the sign bit.
 __device__ __forceinline__ uint32_t score_key(uint32_t bits) {
-  return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+  return bits ^ ((uint32_t)((int32_t)bits >> 31) | 0x80000000u);
 }
 
 // Inverse of score_key: the original fp32 bits.
 __device__ __forceinline__ uint32_t score_bits(uint32_t key) {
-  return (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
+  return key ^ ((uint32_t)((int32_t)~key >> 31) | 0x80000000u);
 }
 
 struct SelectShared {
