@@ -52,6 +52,8 @@ def _load():
             lib.oracle_merge.argtypes = [P, P, I, I, I, P, P, P]
             lib.oracle_local_topk.argtypes = [P, I, I, I, I, I, I, P, P, P]
             lib.oracle_fused_topk.argtypes = [P, I, I, I, I, I, P, P, P]
+            lib.oracle_local_topk_ids.argtypes = [P, I, I, I, I, I, I, P, I, P, P]
+            lib.oracle_fused_topk_ids.argtypes = [P, I, I, I, I, I, P, I, P, P]
             for f in (lib.oracle_merge_rows, lib.oracle_merge, lib.oracle_local_topk,
                       lib.oracle_fused_topk):
                 f.restype = ctypes.c_int
@@ -89,9 +91,11 @@ def merge(scores, ids, row_starts=None, rows=None):
     return out_ids, out_scores
 
 
-def local_topk(logits, K, rank, dcp, L=None, row_starts=None):
+def local_topk(logits, K, rank, dcp, L=None, row_starts=None, interleaved=False):
     """One rank's top-K over logits rows ``(T, ld)`` (first ``L`` columns).
 
+    Ids are ``row_starts + rank*L + c`` (contiguous shards) or, with
+    ``interleaved``, ``row_starts + c*dcp + rank``.
     Returns ``(out_scores, out_ids)``, each ``(T, K)``.
     """
     logits = _c(logits, np.float32)
@@ -100,15 +104,16 @@ def local_topk(logits, K, rank, dcp, L=None, row_starts=None):
     rs = _c(row_starts, np.int32)
     out_scores = np.empty((T, K), np.float32)
     out_ids = np.empty((T, K), np.int32)
-    rc = _load().oracle_local_topk(_ptr(logits), T, L, ld, K, rank, dcp, _ptr(rs),
-                                   _ptr(out_scores), _ptr(out_ids))
+    rc = _load().oracle_local_topk_ids(_ptr(logits), T, L, ld, K, rank, dcp, _ptr(rs),
+                                       int(bool(interleaved)), _ptr(out_scores), _ptr(out_ids))
     if rc != 0:
-        raise ValueError(f"oracle_local_topk failed with {rc}")
+        raise ValueError(f"oracle_local_topk_ids failed with {rc}")
     return out_scores, out_ids
 
 
-def fused_topk(logits, K, L=None, row_starts=None):
-    """Top-K over all shards' logits ``(dcp, T, ld)`` at once.
+def fused_topk(logits, K, L=None, row_starts=None, interleaved=False):
+    """Top-K over all shards' logits ``(dcp, T, ld)`` at once, ids as in
+    ``local_topk``.
 
     Returns ``(out_scores, out_ids)``, each ``(T, K)``.
     """
@@ -118,8 +123,8 @@ def fused_topk(logits, K, L=None, row_starts=None):
     rs = _c(row_starts, np.int32)
     out_scores = np.empty((T, K), np.float32)
     out_ids = np.empty((T, K), np.int32)
-    rc = _load().oracle_fused_topk(_ptr(logits), T, dcp, L, ld, K, _ptr(rs),
-                                   _ptr(out_scores), _ptr(out_ids))
+    rc = _load().oracle_fused_topk_ids(_ptr(logits), T, dcp, L, ld, K, _ptr(rs),
+                                       int(bool(interleaved)), _ptr(out_scores), _ptr(out_ids))
     if rc != 0:
-        raise ValueError(f"oracle_fused_topk failed with {rc}")
+        raise ValueError(f"oracle_fused_topk_ids failed with {rc}")
     return out_scores, out_ids

@@ -29,8 +29,9 @@
  *  - the output is the K winners in key order, scores copied bit for bit;
  *  - row_starts[t] (0 when absent) is added to every non-padding output id of
  *    the merge, and to every id the local top-K emits;
- *  - local top-K ids are row_starts[t] + rank*L + column, and rows with fewer
- *    than K columns are padded with (-inf, -1).
+ *  - local top-K ids are row_starts[t] + rank*L + column (contiguous shards,
+ *    the default) or row_starts[t] + column*dcp + rank (interleaved shards),
+ *    and rows with fewer than K columns are padded with (-inf, -1).
  *
  * Parity is pinned for every exported function (hand-worked examples, brute
  * force on tiny inputs, invariants, the local/merge composition identity).
@@ -129,10 +130,23 @@ int oracle_merge(const float* scores, const int32_t* ids, int T, int dcp, int K,
     return oracle_merge_rows(scores, ids, T, dcp, K, row_starts, NULL, T, out_ids, out_scores);
 }
 
-int oracle_local_topk(const float* logits, int T, int L, int ld, int K, int rank, int dcp,
-                      const int32_t* row_starts, float* out_scores, int32_t* out_ids)
+/* Global id (before row_starts) of column c of rank r's shard: contiguous
+ * shards own [r*L, (r+1)*L); interleaved shards own the ids = r (mod dcp),
+ * column c being id c*dcp + r. */
+static uint32_t shard_id(int interleaved, int r, int dcp, int L, int c)
 {
-    if (T < 0 || L < 1 || ld < L || K < 1 || dcp < 1 || rank < 0 || rank >= dcp)
+    if (interleaved)
+        return (uint32_t)c * (uint32_t)dcp + (uint32_t)r;
+    return (uint32_t)r * (uint32_t)L + (uint32_t)c;
+}
+
+int oracle_local_topk_ids(const float* logits, int T, int L, int ld, int K, int rank, int dcp,
+                          const int32_t* row_starts, int interleaved, float* out_scores,
+                          int32_t* out_ids)
+{
+    /* Rank `rank`'s top-K over its L columns, ordered by (score, global id). */
+    if (T < 0 || L < 1 || ld < L || K < 1 || dcp < 1 || rank < 0 || rank >= dcp ||
+        (interleaved != 0 && interleaved != 1))
         return 1;
     if (T == 0)
         return 0;
@@ -142,17 +156,69 @@ int oracle_local_topk(const float* logits, int T, int L, int ld, int K, int rank
     for (int t = 0; t < T; ++t) {
         const float* row = logits + (int64_t)t * ld;
         for (int c = 0; c < L; ++c) {
+            const uint32_t gid = shard_id(interleaved, rank, dcp, L, c);
             buf[c].score = row[c];
-            buf[c].id = c;
-            buf[c].key = cand_key(row[c], (uint32_t)c);
+            buf[c].id = (int32_t)gid;
+            buf[c].key = cand_key(row[c], gid);
             buf[c].pos = c;
         }
         qsort(buf, (size_t)L, sizeof(cand_t), by_key_desc);
-        const int32_t base = (row_starts ? row_starts[t] : 0) + rank * L;
+        const uint32_t base = row_starts ? (uint32_t)row_starts[t] : 0u;
         for (int j = 0; j < K; ++j) {
             if (j < L) {
                 out_scores[(int64_t)t * K + j] = buf[j].score;
-                out_ids[(int64_t)t * K + j] = base + buf[j].id;
+                out_ids[(int64_t)t * K + j] = (int32_t)(base + (uint32_t)buf[j].id);
+            } else {
+                out_scores[(int64_t)t * K + j] = -INFINITY;
+                out_ids[(int64_t)t * K + j] = -1;
+            }
+        }
+    }
+    free(buf);
+    return 0;
+}
+
+int oracle_local_topk(const float* logits, int T, int L, int ld, int K, int rank, int dcp,
+                      const int32_t* row_starts, float* out_scores, int32_t* out_ids)
+{
+    return oracle_local_topk_ids(logits, T, L, ld, K, rank, dcp, row_starts, 0, out_scores,
+                                 out_ids);
+}
+
+int oracle_fused_topk_ids(const float* logits, int T, int dcp, int L, int ld, int K,
+                          const int32_t* row_starts, int interleaved, float* out_scores,
+                          int32_t* out_ids)
+{
+    /* Top-K taken directly over all dcp*L logits of a row, global id
+     * row_starts[t] + shard_id(r, c): the result the local top-K followed by
+     * the merge must reproduce. */
+    if (T < 0 || dcp < 1 || L < 1 || ld < L || K < 1 || (interleaved != 0 && interleaved != 1))
+        return 1;
+    if (T == 0)
+        return 0;
+    const int64_t n = (int64_t)dcp * L;
+    cand_t* buf = (cand_t*)malloc(sizeof(cand_t) * (size_t)n);
+    if (!buf)
+        return 2;
+    for (int t = 0; t < T; ++t) {
+        int64_t m = 0;
+        for (int r = 0; r < dcp; ++r) {
+            const float* row = logits + ((int64_t)r * T + t) * ld;
+            for (int c = 0; c < L; ++c) {
+                const uint32_t gid = shard_id(interleaved, r, dcp, L, c);
+                buf[m].score = row[c];
+                buf[m].id = (int32_t)gid;
+                buf[m].key = cand_key(row[c], gid);
+                buf[m].pos = m;
+                ++m;
+            }
+        }
+        qsort(buf, (size_t)n, sizeof(cand_t), by_key_desc);
+        const uint32_t base = row_starts ? (uint32_t)row_starts[t] : 0u;
+        for (int j = 0; j < K; ++j) {
+            if (j < n) {
+                out_scores[(int64_t)t * K + j] = buf[j].score;
+                out_ids[(int64_t)t * K + j] = (int32_t)(base + (uint32_t)buf[j].id);
             } else {
                 out_scores[(int64_t)t * K + j] = -INFINITY;
                 out_ids[(int64_t)t * K + j] = -1;
@@ -166,42 +232,5 @@ int oracle_local_topk(const float* logits, int T, int L, int ld, int K, int rank
 int oracle_fused_topk(const float* logits, int T, int dcp, int L, int ld, int K,
                       const int32_t* row_starts, float* out_scores, int32_t* out_ids)
 {
-    /* Top-K taken directly over all dcp*L logits of a row, global id
-     * row_starts[t] + r*L + c: the result the local top-K followed by the
-     * merge must reproduce. */
-    if (T < 0 || dcp < 1 || L < 1 || ld < L || K < 1)
-        return 1;
-    if (T == 0)
-        return 0;
-    const int64_t n = (int64_t)dcp * L;
-    cand_t* buf = (cand_t*)malloc(sizeof(cand_t) * (size_t)n);
-    if (!buf)
-        return 2;
-    for (int t = 0; t < T; ++t) {
-        int64_t m = 0;
-        for (int r = 0; r < dcp; ++r) {
-            const float* row = logits + ((int64_t)r * T + t) * ld;
-            for (int c = 0; c < L; ++c) {
-                const uint32_t gid = (uint32_t)r * (uint32_t)L + (uint32_t)c;
-                buf[m].score = row[c];
-                buf[m].id = (int32_t)gid;
-                buf[m].key = cand_key(row[c], gid);
-                buf[m].pos = m;
-                ++m;
-            }
-        }
-        qsort(buf, (size_t)n, sizeof(cand_t), by_key_desc);
-        const int32_t base = row_starts ? row_starts[t] : 0;
-        for (int j = 0; j < K; ++j) {
-            if (j < n) {
-                out_scores[(int64_t)t * K + j] = buf[j].score;
-                out_ids[(int64_t)t * K + j] = base + buf[j].id;
-            } else {
-                out_scores[(int64_t)t * K + j] = -INFINITY;
-                out_ids[(int64_t)t * K + j] = -1;
-            }
-        }
-    }
-    free(buf);
-    return 0;
+    return oracle_fused_topk_ids(logits, T, dcp, L, ld, K, row_starts, 0, out_scores, out_ids);
 }

@@ -29,6 +29,15 @@ int oracle_local_topk(const float* logits, int T, int L, int ld, int K, int rank
 int oracle_fused_topk(const float* logits, int T, int dcp, int L, int ld, int K,
                       const int32_t* row_starts, float* out_scores, int32_t* out_ids);
 
+/* The same two with the shard id layout chosen: interleaved = 0 gives ids
+ * r*L + c (contiguous shards), interleaved = 1 gives ids c*dcp + r. */
+int oracle_local_topk_ids(const float* logits, int T, int L, int ld, int K, int rank, int dcp,
+                          const int32_t* row_starts, int interleaved, float* out_scores,
+                          int32_t* out_ids);
+int oracle_fused_topk_ids(const float* logits, int T, int dcp, int L, int ld, int K,
+                          const int32_t* row_starts, int interleaved, float* out_scores,
+                          int32_t* out_ids);
+
 #ifdef __cplusplus
 }
 #endif

@@ -61,8 +61,10 @@ def parse_local_examples(path=os.path.join(GOLDEN, "local_examples.txt")):
             continue
         head, _, rest = line.partition(" ")
         if head == "example":
-            cur = {"name": rest, "row_starts": None}
+            cur = {"name": rest, "row_starts": None, "interleaved": False}
             out.append(cur)
+        elif head == "layout":
+            cur["interleaved"] = rest.strip() == "interleaved"
         elif head == "L":
             a = rest.split()
             cur["L"] = int(a[0])
@@ -77,6 +79,37 @@ def parse_local_examples(path=os.path.join(GOLDEN, "local_examples.txt")):
             cur["ids"] = [int(x) for x in rest.split()]
         elif head == "scores":
             cur["scores"] = [_f(x) for x in rest.split()]
+    return out
+
+
+def parse_fused_examples(path=os.path.join(GOLDEN, "fused_examples.txt")):
+    out = []
+    cur = None
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        head, _, rest = line.partition(" ")
+        if head == "example":
+            cur = {"name": rest, "row_starts": None, "shards": []}
+            out.append(cur)
+        elif head == "dcp":
+            a = rest.split()
+            cur["dcp"], cur["L"], cur["K"] = int(a[0]), int(a[2]), int(a[4])
+        elif head == "layout":
+            cur["interleaved"] = rest.strip() == "interleaved"
+        elif head == "shard":
+            _, _, vals = rest.partition(":")
+            cur["shards"].append([_f(x) for x in vals.split()])
+        elif head == "row_starts":
+            cur["row_starts"] = int(rest)
+        elif head == "ids":
+            cur["ids"] = [int(x) for x in rest.split()]
+        elif head == "scores":
+            cur["scores"] = [_f(x) for x in rest.split()]
+    for ex in out:
+        assert len(ex["shards"]) == ex["dcp"] and all(len(r) == ex["L"] for r in ex["shards"])
+        ex["logits"] = np.array([[r] for r in ex["shards"]], np.float32)  # (dcp, 1, L)
     return out
 
 

@@ -10,7 +10,10 @@ mathematics rather than by the oracle itself:
 * permutation invariance over every arrangement of the candidates;
 * row independence (the second page's chunking claim);
 * the composition identity: per-shard local top-K followed by the merge
-  equals the top-K over all shards' logits at once.
+  equals the top-K over all shards' logits at once, with contiguous and with
+  interleaved shard ids;
+* the two shard id layouts give different, hand-worked orders
+  (tests/golden/fused_examples.txt).
 
 A plausible mistake in the oracle (a missing inversion of negative keys, a
 signed instead of unsigned id order, row_starts on padding, a dropped shard,
@@ -42,7 +45,17 @@ def test_merge_golden(ex):
 def test_local_golden(ex):
     rs = None if ex["row_starts"] is None else np.array([ex["row_starts"]], np.int32)
     out_scores, out_ids = oracle.local_topk(ex["row"], ex["K"], ex["rank"], ex["dcp"],
-                                            L=ex["L"], row_starts=rs)
+                                            L=ex["L"], row_starts=rs,
+                                            interleaved=ex["interleaved"])
+    assert out_ids[0].tolist() == ex["ids"]
+    assert np.array_equal(_bits(out_scores[0]), _bits(np.array(ex["scores"], np.float32)))
+
+
+@pytest.mark.parametrize("ex", helpers.parse_fused_examples(), ids=lambda e: e["name"])
+def test_fused_golden(ex):
+    rs = None if ex["row_starts"] is None else np.array([ex["row_starts"]], np.int32)
+    out_scores, out_ids = oracle.fused_topk(ex["logits"], ex["K"], row_starts=rs,
+                                            interleaved=ex["interleaved"])
     assert out_ids[0].tolist() == ex["ids"]
     assert np.array_equal(_bits(out_scores[0]), _bits(np.array(ex["scores"], np.float32)))
 
@@ -99,11 +112,14 @@ def test_local_brute_force(seed):
     K = int(rng.integers(1, 6))
     dcp = int(rng.integers(1, 4))
     rank = int(rng.integers(0, dcp))
+    inter = seed % 2 == 1
     row = np.array([POOL[i] for i in rng.integers(0, len(POOL), ld)], np.float32)[None, :]
     rs = np.array([int(rng.integers(0, 500))], np.int32)
-    out_scores, out_ids = oracle.local_topk(row, K, rank, dcp, L=L, row_starts=rs)
-    base = int(rs[0]) + rank * L
-    cands = [(float(row[0, c]), base + c) for c in range(L)]
+    out_scores, out_ids = oracle.local_topk(row, K, rank, dcp, L=L, row_starts=rs,
+                                            interleaved=inter)
+    rs0 = int(rs[0])
+    cands = [(float(row[0, c]), rs0 + (c * dcp + rank if inter else rank * L + c))
+             for c in range(L)]
     want = helpers.brute_force_topk(cands, min(K, L)) + [(-math.inf, -1)] * max(0, K - L)
     assert out_ids[0].tolist() == [i for _, i in want]
     assert np.array_equal(_bits(out_scores[0]), _bits(np.array([s for s, _ in want], np.float32)))
@@ -121,33 +137,41 @@ def test_rows_are_independent():
         assert np.array_equal(_bits(sub[1][0]), _bits(full[1][t]))
 
 
+@pytest.mark.parametrize("inter", [False, True], ids=["contiguous", "interleaved"])
 @pytest.mark.parametrize("mode", ["bf16", "ties", "normal"])
-def test_composition_local_then_merge(mode):
+def test_composition_local_then_merge(mode, inter):
     """Every global winner is in its own shard's top-K, and the id map is
-    monotone in the column, so the merge of the per-shard top-K equals the
-    top-K over all shards' logits."""
+    monotone in the column (in both shard layouts), so the merge of the
+    per-shard top-K equals the top-K over all shards' logits."""
     dcp, T, L, K = 4, 3, 96, 40
     rng_logits = np.stack([workloads.random_logits(50 + r, T, L, mode=mode) for r in range(dcp)])
     rs = np.array([0, 7, 1000], np.int32)
     loc_s = np.empty((dcp, T, K), np.float32)
     loc_i = np.empty((dcp, T, K), np.int32)
     for r in range(dcp):
-        loc_s[r], loc_i[r] = oracle.local_topk(rng_logits[r], K, r, dcp, row_starts=None)
+        loc_s[r], loc_i[r] = oracle.local_topk(rng_logits[r], K, r, dcp, row_starts=None,
+                                               interleaved=inter)
     m_ids, m_scores = oracle.merge(loc_s, loc_i, rs)
-    f_scores, f_ids = oracle.fused_topk(rng_logits, K, row_starts=rs)
+    f_scores, f_ids = oracle.fused_topk(rng_logits, K, row_starts=rs, interleaved=inter)
     assert np.array_equal(m_ids, f_ids)
     assert np.array_equal(_bits(m_scores), _bits(f_scores))
 
 
-def test_fused_equals_brute_force():
-    rng = np.random.default_rng(77)
-    dcp, L, K = 2, 3, 4
+@pytest.mark.parametrize("seed", range(12))
+def test_fused_equals_brute_force(seed):
+    rng = np.random.default_rng(77 + seed)
+    dcp = int(rng.integers(1, 4))
+    L = int(rng.integers(1, 4))
+    K = int(rng.integers(1, 5))
+    inter = seed % 2 == 1
     logits = np.array([POOL[i] for i in rng.integers(0, len(POOL), dcp * L)],
                       np.float32).reshape(dcp, 1, L)
-    out_scores, out_ids = oracle.fused_topk(logits, K)
-    cands = [(float(logits[r, 0, c]), r * L + c) for r in range(dcp) for c in range(L)]
-    want = helpers.brute_force_topk(cands, K)
+    out_scores, out_ids = oracle.fused_topk(logits, K, interleaved=inter)
+    cands = [(float(logits[r, 0, c]), c * dcp + r if inter else r * L + c)
+             for r in range(dcp) for c in range(L)]
+    want = helpers.brute_force_topk(cands, min(K, dcp * L)) + [(-math.inf, -1)] * max(0, K - dcp * L)
     assert out_ids[0].tolist() == [i for _, i in want]
+    assert np.array_equal(_bits(out_scores[0]), _bits(np.array([s for s, _ in want], np.float32)))
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "tieheavy"])
