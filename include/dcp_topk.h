@@ -151,6 +151,40 @@ dcp_status dcp_fused_topk(const float* logits, int T, int dcp, int L, int ld, in
                           dcp_stream_t stream);
 
 /*
+ * Shard id layouts for the local and fused top-K.  The pages do not fix how a
+ * rank's local KV positions map to global token ids:
+ *   DCP_IDS_CONTIGUOUS   column c of rank r is id r*L + c (shard r owns
+ *                        [r*L, (r+1)*L)); what dcp_local_topk and
+ *                        dcp_fused_topk use.
+ *   DCP_IDS_INTERLEAVED  column c of rank r is id c*dcp + r (tokens dealt to
+ *                        the ranks round-robin).
+ * In both the id grows with the column within a shard, so the local top-K of
+ * every shard followed by dcp_topk_merge still equals the fused top-K.
+ */
+typedef enum { DCP_IDS_CONTIGUOUS = 0, DCP_IDS_INTERLEAVED = 1 } dcp_id_layout;
+
+/*
+ * dcp_local_topk_ex -- dcp_local_topk with the shard id layout chosen:
+ * out_ids are row_starts[t] + rank*L + column (DCP_IDS_CONTIGUOUS) or
+ * row_starts[t] + column*dcp + rank (DCP_IDS_INTERLEAVED).  Among equal
+ * scores the lower id ranks first.  Other arguments and errors as
+ * dcp_local_topk; a layout outside the enum is DCP_ERR_INVALID.
+ */
+dcp_status dcp_local_topk_ex(const float* logits, int T, int L, int ld, int K, int rank, int dcp,
+                             const int32_t* row_starts, int layout, float* out_scores,
+                             int32_t* out_ids, dcp_stream_t stream);
+
+/*
+ * dcp_fused_topk_ex -- dcp_fused_topk with the shard id layout chosen: ids are
+ * row_starts[t] + r*L + column or row_starts[t] + column*dcp + r, and among
+ * equal scores the lower id ranks first.  Other arguments and errors as
+ * dcp_fused_topk; a layout outside the enum is DCP_ERR_INVALID.
+ */
+dcp_status dcp_fused_topk_ex(const float* logits, int T, int dcp, int L, int ld, int K,
+                             const int32_t* row_starts, int layout, float* out_scores,
+                             int32_t* out_ids, dcp_stream_t stream);
+
+/*
  * dcp_topk_device_status -- reads and clears the device-side status word of
  * the current device.  Kernels that stage rows with bulk copies wait for each
  * copy with a bounded poll (about a second); if a copy never lands, the

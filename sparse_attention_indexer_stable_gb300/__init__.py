@@ -23,7 +23,8 @@ __all__ = [
     "DCP_MAX_K", "DCP_MAX_CANDIDATES", "DcpError",
     "dcp_topk_merge", "dcp_topk_merge_workspace_size", "dcp_local_topk", "dcp_status_string",
     "dcp_fused_topk", "dcp_topk_device_status", "dcp_topk_selftest_wait_timeout",
-    "DCP_DEVICE_COPY_TIMEOUT", "fused_topk",
+    "DCP_DEVICE_COPY_TIMEOUT", "fused_topk", "dcp_local_topk_ex", "dcp_fused_topk_ex",
+    "DCP_IDS_CONTIGUOUS", "DCP_IDS_INTERLEAVED",
     "merge", "local_topk", "library", "library_path",
 ]
 
@@ -31,6 +32,7 @@ DCP_OK, DCP_ERR_INVALID, DCP_ERR_UNSUPPORTED, DCP_ERR_CUDA = 0, 1, 2, 3
 DCP_MAX_K = 4096
 DCP_MAX_CANDIDATES = 16384
 DCP_DEVICE_COPY_TIMEOUT = 1
+DCP_IDS_CONTIGUOUS, DCP_IDS_INTERLEAVED = 0, 1
 
 _lock = threading.Lock()
 _lib = None
@@ -66,6 +68,10 @@ def library():
             lib.dcp_local_topk.restype = I
             lib.dcp_fused_topk.argtypes = [P, I, I, I, I, I, P, P, P, P]
             lib.dcp_fused_topk.restype = I
+            lib.dcp_local_topk_ex.argtypes = [P, I, I, I, I, I, I, P, I, P, P, P]
+            lib.dcp_local_topk_ex.restype = I
+            lib.dcp_fused_topk_ex.argtypes = [P, I, I, I, I, I, P, I, P, P, P]
+            lib.dcp_fused_topk_ex.restype = I
             lib.dcp_topk_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
             lib.dcp_topk_device_status.restype = I
             lib.dcp_topk_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
@@ -105,6 +111,18 @@ def dcp_fused_topk(logits, T, dcp, L, ld, K, row_starts, out_scores, out_ids,
                    stream=None) -> int:
     return library().dcp_fused_topk(logits, T, dcp, L, ld, K, row_starts, out_scores, out_ids,
                                     stream)
+
+
+def dcp_local_topk_ex(logits, T, L, ld, K, rank, dcp, row_starts, layout, out_scores, out_ids,
+                      stream=None) -> int:
+    return library().dcp_local_topk_ex(logits, T, L, ld, K, rank, dcp, row_starts, layout,
+                                       out_scores, out_ids, stream)
+
+
+def dcp_fused_topk_ex(logits, T, dcp, L, ld, K, row_starts, layout, out_scores, out_ids,
+                      stream=None) -> int:
+    return library().dcp_fused_topk_ex(logits, T, dcp, L, ld, K, row_starts, layout, out_scores,
+                                       out_ids, stream)
 
 
 def dcp_topk_device_status():
@@ -181,13 +199,22 @@ def merge(scores, ids, row_starts=None, out_ids=None, out_scores=None, stream=No
     return out_ids, out_scores
 
 
+def _layout(layout):
+    if layout in (DCP_IDS_CONTIGUOUS, "contiguous"):
+        return DCP_IDS_CONTIGUOUS
+    if layout in (DCP_IDS_INTERLEAVED, "interleaved"):
+        return DCP_IDS_INTERLEAVED
+    raise ValueError(f"unknown shard id layout {layout!r}")
+
+
 def local_topk(logits, K, rank, dcp, L=None, row_starts=None, out_scores=None, out_ids=None,
-               stream=None):
+               stream=None, layout="contiguous"):
     """One rank's top-K over its logits rows.
 
     logits: float32 (T, ld) CUDA tensor with unit column stride (row stride
-    ld >= L); the first L columns are the rank's shard.  Returns
-    (out_scores float32 (T, K), out_ids int32 (T, K)).
+    ld >= L); the first L columns are the rank's shard.  layout: "contiguous"
+    (ids row_starts + rank*L + c) or "interleaved" (row_starts + c*dcp + rank).
+    Returns (out_scores float32 (T, K), out_ids int32 (T, K)).
     """
     torch = _torch()
     if not isinstance(logits, torch.Tensor) or logits.dtype != torch.float32 or not logits.is_cuda:
@@ -213,20 +240,22 @@ def local_topk(logits, K, rank, dcp, L=None, row_starts=None, out_scores=None, o
     if out_ids.shape != (T, K) or out_scores.shape != (T, K):
         raise ValueError("outputs must be (T, K)")
     with torch.cuda.device(dev):
-        st = dcp_local_topk(logits.data_ptr(), T, L, ld, K, rank, dcp,
-                            None if row_starts is None else row_starts.data_ptr(),
-                            out_scores.data_ptr(), out_ids.data_ptr(), _stream_handle(stream))
+        st = dcp_local_topk_ex(logits.data_ptr(), T, L, ld, K, rank, dcp,
+                               None if row_starts is None else row_starts.data_ptr(),
+                               _layout(layout), out_scores.data_ptr(), out_ids.data_ptr(),
+                               _stream_handle(stream))
     if st != DCP_OK:
-        raise DcpError(st, "dcp_local_topk")
+        raise DcpError(st, "dcp_local_topk_ex")
     return out_scores, out_ids
 
 
-def fused_topk(logits, K, L=None, row_starts=None, out_scores=None, out_ids=None, stream=None):
+def fused_topk(logits, K, L=None, row_starts=None, out_scores=None, out_ids=None, stream=None,
+               layout="contiguous"):
     """Top-K over all shards' logits at once (local top-K + merge in one pass).
 
     logits: float32 (dcp, T, ld) CUDA tensor, contiguous in its last two dims;
-    the first L columns of each row are candidates.  Returns
-    (out_scores float32 (T, K), out_ids int32 (T, K)).
+    the first L columns of each row are candidates.  layout as for
+    local_topk.  Returns (out_scores float32 (T, K), out_ids int32 (T, K)).
     """
     torch = _torch()
     if not isinstance(logits, torch.Tensor) or logits.dtype != torch.float32 or not logits.is_cuda:
@@ -251,9 +280,10 @@ def fused_topk(logits, K, L=None, row_starts=None, out_scores=None, out_ids=None
     if out_ids.shape != (T, K) or out_scores.shape != (T, K):
         raise ValueError("outputs must be (T, K)")
     with torch.cuda.device(dev):
-        st = dcp_fused_topk(logits.data_ptr(), T, dcp, L, ld, K,
-                            None if row_starts is None else row_starts.data_ptr(),
-                            out_scores.data_ptr(), out_ids.data_ptr(), _stream_handle(stream))
+        st = dcp_fused_topk_ex(logits.data_ptr(), T, dcp, L, ld, K,
+                               None if row_starts is None else row_starts.data_ptr(),
+                               _layout(layout), out_scores.data_ptr(), out_ids.data_ptr(),
+                               _stream_handle(stream))
     if st != DCP_OK:
-        raise DcpError(st, "dcp_fused_topk")
+        raise DcpError(st, "dcp_fused_topk_ex")
     return out_scores, out_ids

@@ -126,11 +126,16 @@ struct MergeSource {
   }
 };
 
+// Column c of one rank's shard is candidate c (ordered by ~c: the global id
+// grows with the column in both shard layouts); its global id is
+// row_starts[t] + id_offset + c*id_stride.
 struct LocalSource {
   const float* logits;
   const int32_t* row_starts;
   int L, ld, rank;
   bool vec4;
+  uint32_t id_offset;  // rank*L (contiguous shards) or rank (interleaved)
+  uint32_t id_stride;  // 1 (contiguous) or dcp (interleaved)
 
   __device__ int count() const { return L; }
 
@@ -170,7 +175,7 @@ struct LocalSource {
   }
 
   __device__ uint32_t row_base(int t) const {
-    return (row_starts ? (uint32_t)__ldg(row_starts + t) : 0u) + (uint32_t)rank * (uint32_t)L;
+    return (row_starts ? (uint32_t)__ldg(row_starts + t) : 0u) + id_offset;
   }
 
   __device__ void prefetch_l2(int t) const {
@@ -183,15 +188,10 @@ struct LocalSource {
   __device__ uint32_t inv_global(int, int i) const { return ~(uint32_t)i; }
 
   __device__ int32_t out_id_from(uint32_t base, uint32_t inv) const {
-    return (int32_t)(base + ~inv);
+    return (int32_t)(base + ~inv * id_stride);
   }
 
-  __device__ int32_t out_id(int t, uint32_t inv) const {
-    const uint32_t c = ~inv;
-    const uint32_t base = (row_starts ? (uint32_t)__ldg(row_starts + t) : 0u) +
-                          (uint32_t)rank * (uint32_t)L;
-    return (int32_t)(base + c);
-  }
+  __device__ int32_t out_id(int t, uint32_t inv) const { return out_id_from(row_base(t), inv); }
 };
 
 // All dcp shards' logits of a row at once: candidate i = r*L + c is column c
@@ -203,6 +203,16 @@ struct FusedSource {
   const int32_t* row_starts;
   int T, dcp, L, ld;
   bool vec4;
+  bool interleaved;             // ids c*dcp + r instead of r*L + c
+  unsigned long long l_recip;   // ceil(2^32 / L): r = (i * l_recip) >> 32 for i < dcp*L
+
+  // Global id (before row_starts) of candidate i = r*L + c.  The quotient by
+  // multiplication is exact because i*L < 2^32.
+  __device__ uint32_t gid(uint32_t i) const {
+    if (!interleaved) return i;
+    const uint32_t r = (uint32_t)(((unsigned long long)i * l_recip) >> 32);
+    return (i - r * (uint32_t)L) * (uint32_t)dcp + r;
+  }
 
   __device__ int count() const { return dcp * L; }
 
@@ -215,7 +225,7 @@ struct FusedSource {
       const float* rp = row(t, r);
       for (int c = threadIdx.x; c < L; c += kThreads) {
         skey[r * L + c] = score_key(__float_as_uint(__ldg(rp + c)));
-        sinv[r * L + c] = ~(uint32_t)(r * L + c);
+        sinv[r * L + c] = ~gid((uint32_t)(r * L + c));
       }
     }
   }
@@ -232,9 +242,11 @@ struct FusedSource {
   }
   __device__ void issue_ids(int, uint32_t*, unsigned long long*) const {}
 
+  // Candidates 4c .. 4c+3 lie in one shard (L % 4 == 0 on this path).
   __device__ uint4 inv4(const uint32_t*, int c) const {
-    const uint32_t i = 4u * (uint32_t)c;
-    return make_uint4(~i, ~(i + 1u), ~(i + 2u), ~(i + 3u));
+    const uint32_t g = gid(4u * (uint32_t)c);
+    const uint32_t d = interleaved ? (uint32_t)dcp : 1u;
+    return make_uint4(~g, ~(g + d), ~(g + 2u * d), ~(g + 3u * d));
   }
 
   __device__ uint32_t row_base(int t) const {
@@ -249,7 +261,7 @@ struct FusedSource {
     const int r = i / L;
     return score_key(__float_as_uint(__ldg(row(t, r) + (i - r * L))));
   }
-  __device__ uint32_t inv_global(int, int i) const { return ~(uint32_t)i; }
+  __device__ uint32_t inv_global(int, int i) const { return ~gid((uint32_t)i); }
 
   __device__ int32_t out_id_from(uint32_t base, uint32_t inv) const {
     return (int32_t)(base + ~inv);
@@ -499,29 +511,62 @@ dcp_status dcp_topk_merge(const float* scores, const int32_t* ids, int T, int dc
   return dcp::launch_rows(src, T, dcp_ * K, K, out_scores, out_ids, (cudaStream_t)stream);
 }
 
-dcp_status dcp_local_topk(const float* logits, int T, int L, int ld, int K, int rank, int dcp_,
-                          const int32_t* row_starts, float* out_scores, int32_t* out_ids,
-                          dcp_stream_t stream) {
-  if (T < 0 || L < 1 || ld < L || K < 1 || dcp_ < 1 || rank < 0 || rank >= dcp_)
+dcp_status dcp_local_topk_ex(const float* logits, int T, int L, int ld, int K, int rank, int dcp_,
+                             const int32_t* row_starts, int layout, float* out_scores,
+                             int32_t* out_ids, dcp_stream_t stream) {
+  if (T < 0 || L < 1 || ld < L || K < 1 || dcp_ < 1 || rank < 0 || rank >= dcp_ ||
+      (layout != DCP_IDS_CONTIGUOUS && layout != DCP_IDS_INTERLEAVED))
     return DCP_ERR_INVALID;
   if (K > DCP_MAX_K || L > DCP_MAX_CANDIDATES) return DCP_ERR_UNSUPPORTED;
   if (T == 0) return DCP_OK;
   if (!logits || !out_scores || !out_ids) return DCP_ERR_INVALID;
-  dcp::LocalSource src{logits, row_starts, L, ld, rank,
-                       (L % 4) == 0 && (ld % 4) == 0 && dcp::aligned16(logits)};
+  dcp::LocalSource src{};
+  src.logits = logits;
+  src.row_starts = row_starts;
+  src.L = L;
+  src.ld = ld;
+  src.rank = rank;
+  src.vec4 = (L % 4) == 0 && (ld % 4) == 0 && dcp::aligned16(logits);
+  const bool inter = layout == DCP_IDS_INTERLEAVED;
+  src.id_offset = inter ? (uint32_t)rank : (uint32_t)rank * (uint32_t)L;
+  src.id_stride = inter ? (uint32_t)dcp_ : 1u;
   return dcp::launch_rows(src, T, L, K, out_scores, out_ids, (cudaStream_t)stream);
+}
+
+dcp_status dcp_local_topk(const float* logits, int T, int L, int ld, int K, int rank, int dcp_,
+                          const int32_t* row_starts, float* out_scores, int32_t* out_ids,
+                          dcp_stream_t stream) {
+  return dcp_local_topk_ex(logits, T, L, ld, K, rank, dcp_, row_starts, DCP_IDS_CONTIGUOUS,
+                           out_scores, out_ids, stream);
+}
+
+dcp_status dcp_fused_topk_ex(const float* logits, int T, int dcp_, int L, int ld, int K,
+                             const int32_t* row_starts, int layout, float* out_scores,
+                             int32_t* out_ids, dcp_stream_t stream) {
+  if (T < 0 || dcp_ < 1 || L < 1 || ld < L || K < 1 ||
+      (layout != DCP_IDS_CONTIGUOUS && layout != DCP_IDS_INTERLEAVED))
+    return DCP_ERR_INVALID;
+  if (K > DCP_MAX_K || (long long)dcp_ * L > DCP_MAX_CANDIDATES) return DCP_ERR_UNSUPPORTED;
+  if (T == 0) return DCP_OK;
+  if (!logits || !out_scores || !out_ids) return DCP_ERR_INVALID;
+  dcp::FusedSource src{};
+  src.logits = logits;
+  src.row_starts = row_starts;
+  src.T = T;
+  src.dcp = dcp_;
+  src.L = L;
+  src.ld = ld;
+  src.vec4 = (L % 4) == 0 && (ld % 4) == 0 && dcp::aligned16(logits);
+  src.interleaved = layout == DCP_IDS_INTERLEAVED;
+  src.l_recip = ((1ull << 32) + (unsigned long long)L - 1ull) / (unsigned long long)L;
+  return dcp::launch_rows(src, T, dcp_ * L, K, out_scores, out_ids, (cudaStream_t)stream);
 }
 
 dcp_status dcp_fused_topk(const float* logits, int T, int dcp_, int L, int ld, int K,
                           const int32_t* row_starts, float* out_scores, int32_t* out_ids,
                           dcp_stream_t stream) {
-  if (T < 0 || dcp_ < 1 || L < 1 || ld < L || K < 1) return DCP_ERR_INVALID;
-  if (K > DCP_MAX_K || (long long)dcp_ * L > DCP_MAX_CANDIDATES) return DCP_ERR_UNSUPPORTED;
-  if (T == 0) return DCP_OK;
-  if (!logits || !out_scores || !out_ids) return DCP_ERR_INVALID;
-  dcp::FusedSource src{logits, row_starts, T, dcp_, L, ld,
-                       (L % 4) == 0 && (ld % 4) == 0 && dcp::aligned16(logits)};
-  return dcp::launch_rows(src, T, dcp_ * L, K, out_scores, out_ids, (cudaStream_t)stream);
+  return dcp_fused_topk_ex(logits, T, dcp_, L, ld, K, row_starts, DCP_IDS_CONTIGUOUS, out_scores,
+                           out_ids, stream);
 }
 
 dcp_status dcp_topk_device_status(unsigned int* status) {

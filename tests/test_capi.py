@@ -106,3 +106,18 @@ def test_device_status_rejects_null():
 ])
 def test_fused_argument_errors(args, want):
     assert dk.dcp_fused_topk(*args, None) == want
+
+
+@pytest.mark.parametrize("layout,want", [(-1, dk.DCP_ERR_INVALID), (2, dk.DCP_ERR_INVALID)])
+def test_layout_argument_errors(layout, want):
+    assert dk.dcp_local_topk_ex(FAKE, 2, 8, 8, 4, 0, 1, None, layout, FAKE, FAKE, None) == want
+    assert dk.dcp_fused_topk_ex(FAKE, 2, 4, 8, 8, 4, None, layout, FAKE, FAKE, None) == want
+    # T == 0 still validates the layout first
+    assert dk.dcp_local_topk_ex(None, 0, 8, 8, 4, 0, 1, None, layout, None, None, None) == want
+
+
+def test_layout_names():
+    assert dk._layout("contiguous") == dk.DCP_IDS_CONTIGUOUS
+    assert dk._layout("interleaved") == dk.DCP_IDS_INTERLEAVED
+    with pytest.raises(ValueError):
+        dk._layout("striped")

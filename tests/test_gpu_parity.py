@@ -313,3 +313,66 @@ def test_sweep_fused(T):
     torch.cuda.synchronize()
     want_s, want_i = oracle.fused_topk(logits, 2048)
     assert_same((out_i.cpu().numpy(), out_s.cpu().numpy()), (want_i, want_s), f"T={T}")
+
+
+# ------------------------------------------------- interleaved shard ids
+INTERLEAVED_LOCAL = [
+    # (T, L, ld, K, rank, dcp, mode)
+    (4, 4096, 4096, 2048, 2, 4, "bf16"),
+    (3, 1000, 1003, 64, 1, 3, "ties"),
+    (2, 100, 100, 200, 0, 2, "normal"),  # L < K: padded
+    (170, 4096, 4096, 2048, 3, 4, "ties"),  # more rows than SMs
+]
+
+
+@pytest.mark.parametrize("case", INTERLEAVED_LOCAL, ids=lambda c: "-".join(map(str, c)))
+def test_local_topk_interleaved(case):
+    T, L, ld, K, rank, dcp, mode = case
+    logits = workloads.random_logits(zlib.crc32(repr(case).encode()) & 0xFFFF, T, L, ld=ld, mode=mode)
+    rs = np.arange(T, dtype=np.int32) * 7
+    out_s, out_i = dk.local_topk(_dev(logits), K, rank, dcp, L=L, row_starts=_dev(rs),
+                                 layout="interleaved")
+    torch.cuda.synchronize()
+    want_s, want_i = oracle.local_topk(logits, K, rank, dcp, L=L, row_starts=rs, interleaved=True)
+    assert_same((out_i.cpu().numpy(), out_s.cpu().numpy()), (want_i, want_s), str(case))
+
+
+INTERLEAVED_FUSED = [
+    # (T, dcp, L, ld, K, mode)
+    (4, 4, 4096, 4096, 2048, "bf16"),
+    (3, 4, 4096, 4100, 2048, "ties"),
+    (5, 3, 1000, 1000, 64, "ties"),
+    (2, 3, 1001, 1003, 200, "normal"),  # L % 4 != 0: the general path
+    (160, 4, 4096, 4096, 2048, "bf16"),
+    (2, 2, 8192, 8192, 2048, "ties"),   # 16384 candidates per row
+]
+
+
+@pytest.mark.parametrize("case", INTERLEAVED_FUSED, ids=lambda c: "-".join(map(str, c)))
+def test_fused_topk_interleaved(case):
+    T, dcp, L, ld, K, mode = case
+    seed = zlib.crc32(repr(case).encode()) & 0xFFFF
+    logits = np.stack([workloads.random_logits(seed + r, T, L, ld=ld, mode=mode) for r in range(dcp)])
+    rs = (np.arange(T, dtype=np.int32) * 5) if T % 2 else None
+    out_s, out_i = dk.fused_topk(_dev(logits), K, L=L, row_starts=None if rs is None else _dev(rs),
+                                 layout="interleaved")
+    torch.cuda.synchronize()
+    want_s, want_i = oracle.fused_topk(logits, K, L=L, row_starts=rs, interleaved=True)
+    assert_same((out_i.cpu().numpy(), out_s.cpu().numpy()), (want_i, want_s), str(case))
+
+
+def test_interleaved_local_then_merge():
+    """Interleaved shards: per-shard local top-K on the GPU, then the merge,
+    equals the oracle's fused top-K with interleaved ids."""
+    logits = workloads.sweep_logits(32, seed=11)
+    dcp, T, L = logits.shape
+    K = 2048
+    x = _dev(logits)
+    cand_s = torch.empty((dcp, T, K), dtype=torch.float32, device="cuda")
+    cand_i = torch.empty((dcp, T, K), dtype=torch.int32, device="cuda")
+    for r in range(dcp):
+        dk.local_topk(x[r], K, r, dcp, out_scores=cand_s[r], out_ids=cand_i[r], layout="interleaved")
+    out_ids, out_scores = dk.merge(cand_s, cand_i)
+    torch.cuda.synchronize()
+    want_s, want_i = oracle.fused_topk(logits, K, interleaved=True)
+    assert_same((out_ids.cpu().numpy(), out_scores.cpu().numpy()), (want_i, want_s), "interleaved")
