@@ -9,10 +9,11 @@ per-launch durations come from CUDA events on the launching stream.  Inputs
 (640 MiB) exceed the 129 MB L2, so no flush is needed between launches.
 
 Prints one JSON line (rank 0).  Besides the headline, the line carries the
-decode-size latencies (16 rows: the random and the tie-heavy workload) and the
-local-top-K + merge sweep, the HBM roofline of the merge kernel, the oracle
-timed on the host cores, and an end-to-end number through the Python API with
-host buffers.
+decode-size latencies (16 rows: the random and the tie-heavy workload), the
+selector shapes of the first page's benchmark table (16 rows with 4096, 8192
+and 16384 candidates; 64 and 256 rows with 8192), the local-top-K + merge
+sweep, the HBM roofline of the merge kernel, the oracle timed on the host
+cores, and an end-to-end number through the Python API with host buffers.
 
 ``--impl reference`` times the CPU oracle instead (the only reference this
 method has): a bounded sample of the same workload on the host cores.
@@ -372,6 +373,26 @@ def decode_and_sweep(torch, dk, dev, stream):
         out[f"{name}_T{m.T}_us_per_launch"] = median_of_reps(torch, raw, stream)
         out[f"{name}_T{m.T}_us_per_graph_replay"] = median_of_reps(torch, raw, stream, graph=True)
         out[f"{name}_T{m.T}_us_per_python_call"] = median_of_reps(torch, fn, stream)
+    # the selector shapes of the first page's table (K=2048; candidates dcp*K;
+    # random fp32 scores), timed like the decode merge
+    shapes = {}
+    for T, dcp in ((16, 2), (16, 4), (16, 8), (64, 4), (256, 4)):
+        m = workloads.decode(seed=50 + T + dcp, T=T, dcp=dcp)
+        s = torch.from_numpy(m.scores).to(dev)
+        i = torch.from_numpy(m.ids).to(dev)
+        oi = torch.empty((m.T, m.K), dtype=torch.int32, device=dev)
+        os_ = torch.empty((m.T, m.K), dtype=torch.float32, device=dev)
+        lib = dk.library()
+        args = (s.data_ptr(), i.data_ptr(), m.T, m.dcp, m.K, None, oi.data_ptr(),
+                os_.data_ptr(), None, 0, stream.cuda_stream)
+
+        def raw():
+            lib.dcp_topk_merge(*args)
+
+        shapes[f"rows{T}_candidates{dcp * m.K}"] = {
+            "us_per_launch": median_of_reps(torch, raw, stream),
+            "us_per_graph_replay": median_of_reps(torch, raw, stream, graph=True)}
+    out["selector_shapes_K2048"] = shapes
     sweep = {}
     K = 2048
     for T in workloads.SWEEP_T:
