@@ -87,17 +87,6 @@ struct MergeSource {
     return make_uint4(~w.x, ~w.y, ~w.z, ~w.w);
   }
 
-  // Starts pulling row t's candidates into L2 (one thread; no completion to
-  // wait for: the later 16-byte copies of the row then hit L2).
-  __device__ void prefetch_l2(int t) const {
-    const size_t stride = (size_t)T * (size_t)K;
-    const size_t off = (size_t)t * (size_t)K;
-    for (int r = 0; r < dcp; ++r) {
-      prefetch_l2_bulk(scores + off + r * stride, (uint32_t)K * 4u);
-      prefetch_l2_bulk(ids + off + r * stride, (uint32_t)K * 4u);
-    }
-  }
-
   // Candidate i of row t read from global memory (the fallback path).
   __device__ uint32_t key_global(int t, int i) const {
     const int r = i / K;
@@ -178,9 +167,6 @@ struct LocalSource {
     return (row_starts ? (uint32_t)__ldg(row_starts + t) : 0u) + id_offset;
   }
 
-  __device__ void prefetch_l2(int t) const {
-    prefetch_l2_bulk(logits + (size_t)t * (size_t)ld, (uint32_t)L * 4u);
-  }
 
   __device__ uint32_t key_global(int t, int i) const {
     return score_key(__float_as_uint(__ldg(logits + (size_t)t * (size_t)ld + i)));
@@ -253,9 +239,6 @@ struct FusedSource {
     return row_starts ? (uint32_t)__ldg(row_starts + t) : 0u;
   }
 
-  __device__ void prefetch_l2(int t) const {
-    for (int r = 0; r < dcp; ++r) prefetch_l2_bulk(row(t, r), (uint32_t)L * 4u);
-  }
 
   __device__ uint32_t key_global(int t, int i) const {
     const int r = i / L;

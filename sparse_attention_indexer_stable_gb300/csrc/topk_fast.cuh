@@ -152,11 +152,6 @@ __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
-// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* gmem, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(gmem), "r"(bytes) : "memory");
-}
-
 // Fine buckets for an L1 bin of h candidates: half of h rounded up to a power
 // of two, at least 1 and at most 1024 (0 for an empty bin).  Never more than
 // h, so the bins above b1 (fewer than K candidates) get fewer than K buckets.
@@ -292,7 +287,6 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       src.issue_scores(t, stage, &s.stage_bar);
       if constexpr (Source::kStagesIds) src.issue_ids(t, aux, &s.ids_bar);
     }
-    if (t + G < T) src.prefetch_l2(t + G);
   }
 
   for (uint32_t k = 0; t < T; t += G, ++k) {
@@ -306,11 +300,9 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       if constexpr (Source::kStagesIds) mbar_wait_bounded(&s.ids_bar, k & 1u, kStageWaitLimit);
       return;
     }
-    // Rows stream from HBM into L2 two rows ahead of their use.  The copy of
-    // the next row's scores into the stage starts as soon as this row's are
-    // consumed (after COMPACT); its ids follow at the end of the row (the
+    // The copy of the next row's scores into the stage starts as soon as this
+    // row's are consumed (after L1); its ids follow at the end of the row (the
     // aux region serves RANK until then) and are needed only by COMPACT.
-    if (tid == 0 && t + 2 * G < T) src.prefetch_l2(t + 2 * G);
 
     // ---- L1: histogram of the score keys' top 11 bits ---------------------
     // Also ORs the low 21 bits of every raw score: the bits that are zero in
@@ -338,6 +330,11 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & 0x1FFFFFu);
     if (lane == 0 && raw_or) atomicOr(&s.stat_or[0], raw_or);
     __syncthreads();
+    // L1 was the last reader of the staged scores (the rest of the row works
+    // from the keys in registers, the staged ids and, in the fallback, global
+    // memory): stream the next row's scores in behind the rest of this one.
+    const bool next_issued = t + G < T;
+    if (tid == 0 && next_issued) src.issue_scores(t + G, stage, &s.stage_bar);
 
     // ---- SCAN1: bins high to low; packed (buckets << 16 | candidates) -------
     // A warp whose bins are all empty (most warps: the keys fill a narrow
@@ -386,8 +383,10 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       // COMPACT reads the row's ids: they were copied during L1 and SCAN1
       const bool ids_ok = mbar_wait_bounded(&s.ids_bar, k & 1u, kStageWaitLimit);
       if (__syncthreads_or(!ids_ok)) {
+        // also let the next row's scores, already on their way, land
         if (tid == 0) atomicOr(status, kStatusCopyTimeout);
         mbar_wait_bounded(&s.ids_bar, k & 1u, kStageWaitLimit);
+        if (next_issued) mbar_wait_bounded(&s.stage_bar, (k + 1u) & 1u, kStageWaitLimit);
         return;
       }
     } else {
@@ -465,9 +464,6 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       }
     }
     __syncthreads();
-    // The staged row is consumed (the fallback re-reads its row from global
-    // memory): stream the next row in behind the rest of this one.
-    if (tid == 0 && t + G < T) src.issue_scores(t + G, stage, &s.stage_bar);
 
     // ---- L2: fine bucket of every live candidate ---------------------------
     unsigned long long lkey[kLivePer];
@@ -521,15 +517,24 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     if (fast) {
       // warps whose buckets all lie past the last one only report a zero total
       const bool warp_busy = kFinePer * 32 * warp < nfine;
+      // buckets past nfine are empty (fine is zero there), so no guards
       uint32_t c[kFinePer];
       uint32_t local = 0u, incl = 0u;
+      uint32_t* my = s.fine + kFinePer * tid;
       if (warp_busy) {
+        if constexpr (kFinePer % 2 == 0) {
 #pragma unroll
-        for (int e = 0; e < kFinePer; ++e) {
-          const int g = kFinePer * tid + e;
-          c[e] = g < nfine ? s.fine[g] : 0u;
-          local += c[e];
+          for (int e = 0; e < kFinePer; e += 2) {
+            const uint2 w = *reinterpret_cast<const uint2*>(my + e);
+            c[e] = w.x;
+            c[e + 1] = w.y;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < kFinePer; ++e) c[e] = my[e];
         }
+#pragma unroll
+        for (int e = 0; e < kFinePer; ++e) local += c[e];
         incl = warp_inclusive_scan(local);
       }
       if (lane == 31) s.wa[warp] = incl;
@@ -539,17 +544,23 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         const uint32_t wti = warp_inclusive_scan(wt);
         uint32_t st = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
         uint32_t over = 0u;
+        uint32_t w[kFinePer];
 #pragma unroll
         for (int e = 0; e < kFinePer; ++e) {
-          const int g = kFinePer * tid + e;
-          if (g < nfine) {
-            s.fine[g] = (st << 16) | (min(c[e], 255u) << 8);
-            if (st < (uint32_t)ksel) {
-              if (c[e] > kBigBucket) over = 1u;
-              if ((uint32_t)ksel <= st + c[e]) s.p_end = st + c[e];
-            }
-            st += c[e];
+          w[e] = (st << 16) | (min(c[e], 255u) << 8);
+          if (st < (uint32_t)ksel) {
+            if (c[e] > kBigBucket) over = 1u;
+            if ((uint32_t)ksel <= st + c[e]) s.p_end = st + c[e];
           }
+          st += c[e];
+        }
+        if constexpr (kFinePer % 2 == 0) {
+#pragma unroll
+          for (int e = 0; e < kFinePer; e += 2)
+            *reinterpret_cast<uint2*>(my + e) = make_uint2(w[e], w[e + 1]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < kFinePer; ++e) my[e] = w[e];
         }
         over = __reduce_or_sync(0xFFFFFFFFu, over);
         if (lane == 0 && over) s.overflow = 1u;
