@@ -26,9 +26,9 @@
 //          gathered into the bucket's slice of the live list): its output
 //          position is the bucket start plus that count, and positions >= K
 //          are the losers.  Buckets hold a few members, so this one step both
-//          finishes the selection at the threshold and sorts the winners.  The
-//          row's output is assembled in shared memory and leaves in 16-byte
-//          stores.
+//          finishes the selection at the threshold and sorts the winners.
+//          RANK runs over list positions, so a warp's output positions are
+//          consecutive up to a bucket's size and its stores nearly coalesced.
 //
 // Rows whose live set or buckets come out too large for this (pathologically
 // clustered keys) take the radix-select + sort of topk_core.cuh on the same
@@ -84,8 +84,7 @@ struct StreamShared {
 static_assert(offsetof(StreamShared, live) % 16 == 0, "live must be 16-byte aligned");
 static_assert(offsetof(StreamShared, fine) % 16 == 0, "fine must be 16-byte aligned");
 static_assert(offsetof(StreamShared, u) == offsetof(StreamShared, fine) + sizeof(uint32_t) * kFineMax,
-              "the table must follow fine directly (one region for output staging and reset)");
-static_assert(2 * kStreamMaxK <= kFineMax + kHistBins, "output staging must fit fine + table");
+              "the table must follow fine directly (one region to reset)");
 static_assert(kRankMax >= kStreamMaxK + (int)kBigBucket - 1, "list positions must reach the straddling bucket's end");
 // Scratch for RANK in the aux region: rank keys (u64) then bucket info (u16)
 // per list position.
@@ -571,9 +570,6 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
 
     float* os = out_scores + (size_t)t * (size_t)K;
     int32_t* oi = out_ids + (size_t)t * (size_t)K;
-    // Output staging, once `fine` and the L1 table are no longer read: the
-    // row's scores in words [0, K), its ids in [K, 2K).
-    uint32_t* ostage = s.fine;
     if (fast) {
       // ---- SCATTER: winners' keys into the list, in bucket order -----------
       // Members of buckets that start before K go to their bucket's slots.
@@ -625,13 +621,13 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         }
         const uint32_t fin = st + r;
         if (fin < (uint32_t)ksel) {
-          ostage[fin] = score_bits((uint32_t)(key >> 32));
-          ostage[K + fin] = (uint32_t)src.out_id_from(rbase, (uint32_t)key);
+          os[fin] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
+          oi[fin] = src.out_id_from(rbase, (uint32_t)key);
         }
       }
       for (int j = ksel + tid; j < K; j += NT) {
-        ostage[j] = 0xFF800000u;  // -inf
-        ostage[K + j] = 0xFFFFFFFFu;  // -1
+        os[j] = __uint_as_float(0xFF800000u);  // -inf
+        oi[j] = -1;
       }
     } else {
       // ---- Fallback: radix select + sort, reading the row from global memory -
@@ -659,30 +655,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     if constexpr (Source::kStagesIds)
       if (tid == 0 && t + G < T) src.issue_ids(t + G, aux, &s.ids_bar);
 
-    // Write the staged output (16-byte stores where K and the output rows
-    // allow), zeroing `fine` and the table behind it: each thread zeroes only
-    // the words it copied, so no barrier is needed between the two.
-    constexpr int kRegion = kFineMax + kHistBins;  // fine, then the table
-    const bool vec_out =
-        (K & 3) == 0 && ((reinterpret_cast<uintptr_t>(os) | reinterpret_cast<uintptr_t>(oi)) & 15u) == 0u;
-    if (fast && !vec_out) {
-      for (int j = tid; j < K; j += NT) {
-        os[j] = __uint_as_float(ostage[j]);
-        oi[j] = (int32_t)ostage[K + j];
-      }
-      __syncthreads();
-    }
-    for (int i = 4 * tid; i < kRegion; i += 4 * NT) {
-      uint4* w = reinterpret_cast<uint4*>(s.fine + i);
-      if (fast && vec_out && i < 2 * K) {
-        const uint4 v = *w;
-        if (i < K)
-          *reinterpret_cast<uint4*>(os + i) = v;
-        else
-          *reinterpret_cast<uint4*>(oi + (i - K)) = v;
-      }
-      *w = make_uint4(0u, 0u, 0u, 0u);
-    }
+    zero_words<NT>(s.fine, kFineMax + kHistBins);  // fine and the table behind it
     if (tid == 0) {
       s.live_cursor = 0u;
       s.p_end = 0u;
