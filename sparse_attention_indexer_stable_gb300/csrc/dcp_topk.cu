@@ -399,8 +399,9 @@ static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Launches with programmatic stream serialization: the grid may be scheduled
 // while the stream's previous kernel is still finishing, and waits for it
-// (griddepcontrol.wait, first thing in every kernel here) before touching
-// memory.  Only the launch latency overlaps; the ordering is the stream's.
+// (griddepcontrol.wait, in every thread before its first global memory
+// access) before touching memory.  Only the launch latency and shared-memory
+// set-up overlap; the ordering is the stream's.
 template <typename... KArgs, typename... Args>
 static cudaError_t launch_serialized(void (*kernel)(KArgs...), int grid, int block, size_t smem,
                                      cudaStream_t stream, Args... args) {

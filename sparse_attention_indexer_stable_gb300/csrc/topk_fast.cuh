@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
 
-  grid_dependency_wait();
+  // Shared-memory set-up first: it touches no global memory, so it may run
+  // while the stream's previous kernel is still finishing.
   zero_words<NT>(s.fine, kFineMax + kHistBins);  // fine and the table behind it
   if (tid == 0) {
     s.live_cursor = 0u;
@@ -281,6 +282,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     mbar_fence_init();
   }
   __syncthreads();
+  grid_dependency_wait();  // every thread, before its first global access
   if (tid == 0) {
     if (t < T) {
       src.issue_scores(t, stage, &s.stage_bar);
