@@ -267,16 +267,27 @@ def run_ours(args):
         if dist is not None:
             dist.barrier()
 
-    m = workloads.NAMED[args.workload]()
-    scores = torch.from_numpy(m.scores).to(dev)
-    ids = torch.from_numpy(m.ids).to(dev)
-    rs = torch.from_numpy(m.row_starts).to(dev)
-    out_ids = torch.empty((m.T, m.K), dtype=torch.int32, device=dev)
-    out_scores = torch.empty((m.T, m.K), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
+    if args.workload.startswith("sweep"):
+        # the fused top-K over one sweep size's logits (dcp=4, L=4096, K=2048)
+        T_sw = int(args.workload[len("sweep"):])
+        lg = torch.from_numpy(workloads.sweep_logits(T_sw)).to(dev)
+        m = workloads.FusedShape(T_sw, lg.shape[0], lg.shape[2], 2048)
+        out_ids = torch.empty((m.T, m.K), dtype=torch.int32, device=dev)
+        out_scores = torch.empty((m.T, m.K), dtype=torch.float32, device=dev)
 
-    def step():
-        dk.merge(scores, ids, rs, out_ids=out_ids, out_scores=out_scores, stream=stream)
+        def step():
+            dk.fused_topk(lg, m.K, out_scores=out_scores, out_ids=out_ids, stream=stream)
+    else:
+        m = workloads.NAMED[args.workload]()
+        scores = torch.from_numpy(m.scores).to(dev)
+        ids = torch.from_numpy(m.ids).to(dev)
+        rs = None if m.row_starts is None else torch.from_numpy(m.row_starts).to(dev)
+        out_ids = torch.empty((m.T, m.K), dtype=torch.int32, device=dev)
+        out_scores = torch.empty((m.T, m.K), dtype=torch.float32, device=dev)
+
+        def step():
+            dk.merge(scores, ids, rs, out_ids=out_ids, out_scores=out_scores, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -312,10 +323,10 @@ def run_ours(args):
 
     # end to end through the Python API with host buffers
     e2e = None
-    if not args.skip_extras:
+    if not args.skip_extras and not args.workload.startswith("sweep"):
         e2e = end_to_end(torch, dk, m, dev, stream, steps=max(3, min(20, args.steps)))
     cpu = None
-    if rank == 0 and world == 1 and not args.skip_extras:
+    if rank == 0 and world == 1 and not args.skip_extras and not args.workload.startswith("sweep"):
         v, rows, secs = cpu_oracle_sample(m, budget_s=args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{rows} rows of the prefill workload ({secs:.1f} s), single-threaded "
@@ -335,7 +346,8 @@ def run_ours(args):
             "achieved_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": profiled_traffic(), "algorithmic_bytes": alg_bytes},
+                         "traffic": profiled_traffic() if args.workload == "prefill" else None,
+                         "algorithmic_bytes": alg_bytes},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,
@@ -475,8 +487,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-extras", action="store_true",
                     help="time only the headline step (used for profiling runs)")
-    ap.add_argument("--workload", default="prefill", choices=sorted(workloads.NAMED),
-                    help="the merge workload of the headline step (default: prefill)")
+    ap.add_argument("--workload", default="prefill",
+                    choices=sorted(workloads.NAMED) + [f"sweep{T}" for T in workloads.SWEEP_T],
+                    help="the workload of the headline step (default: prefill); sweepT times "
+                         "the fused top-K over the T-row sweep logits instead of a merge")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

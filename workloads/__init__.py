@@ -127,6 +127,18 @@ def prefill(seed: int = 4, T: int = 8192, dcp: int = 4, K: int = 2048) -> Merge:
 NAMED = {"tiny": tiny, "decode": decode, "tieheavy": tieheavy, "prefill": prefill}
 
 
+class FusedShape:
+    """Sizes of a fused top-K over per-shard logits (dcp, T, L), K outputs."""
+
+    def __init__(self, T, dcp, L, K):
+        self.T, self.dcp, self.L, self.K = T, dcp, L, K
+        self.row_starts = None
+
+    def algorithmic_bytes(self):
+        """Every logit once, plus the K output (id, score) pairs per row."""
+        return self.T * (self.dcp * self.L * 4 + self.K * 8)
+
+
 def random_merge(seed: int, T: int, dcp: int, K: int, mode: str = "normal",
                  pad_frac: float = 0.0, with_row_starts: bool = False) -> Merge:
     """Small random merge problems for parity sweeps.
