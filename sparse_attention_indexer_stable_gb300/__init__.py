@@ -51,6 +51,8 @@ def library_path() -> str:
 def library():
     """Load (building first if missing or stale) the CUDA library."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             path = _build.LIB_PATH
@@ -144,15 +146,22 @@ def _torch():
     return torch
 
 
-def _stream_handle(stream):
-    torch = _torch()
+def _stream_handle(stream, dev=None):
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = _torch().cuda.current_stream(dev)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ok(t, dtype, device):
+    """Fast form of _check: True when t needs no complaint."""
+    return (t.dtype == dtype and t.is_cuda and t.is_contiguous()
+            and (device is None or t.device == device))
 
 
 def _check(t, name, dtype, device):
     torch = _torch()
+    if isinstance(t, torch.Tensor) and _ok(t, dtype, device):
+        return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
@@ -161,6 +170,15 @@ def _check(t, name, dtype, device):
         raise ValueError(f"{name} must be on {device or 'a CUDA device'}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _on_device(dev, fn):
+    """Run fn with dev current (the library works on the current device)."""
+    torch = _torch()
+    if dev.index == torch.cuda.current_device():
+        return fn()
+    with torch.cuda.device(dev):
+        return fn()
 
 
 def merge(scores, ids, row_starts=None, out_ids=None, out_scores=None, stream=None):
@@ -189,11 +207,11 @@ def merge(scores, ids, row_starts=None, out_ids=None, out_scores=None, stream=No
     _check(out_scores, "out_scores", torch.float32, dev)
     if out_ids.shape != (T, K) or out_scores.shape != (T, K):
         raise ValueError("outputs must be (T, K)")
-    with torch.cuda.device(dev):
-        st = dcp_topk_merge(scores.data_ptr(), ids.data_ptr(), T, dcp, K,
-                            None if row_starts is None else row_starts.data_ptr(),
-                            out_ids.data_ptr(), out_scores.data_ptr(), None, 0,
-                            _stream_handle(stream))
+    st = _on_device(dev, lambda: library().dcp_topk_merge(
+        scores.data_ptr(), ids.data_ptr(), T, dcp, K,
+        None if row_starts is None else row_starts.data_ptr(),
+        out_ids.data_ptr(), out_scores.data_ptr(), None, 0,
+        _stream_handle(stream, dev)))
     if st != DCP_OK:
         raise DcpError(st, "dcp_topk_merge")
     return out_ids, out_scores
@@ -239,11 +257,11 @@ def local_topk(logits, K, rank, dcp, L=None, row_starts=None, out_scores=None, o
     _check(out_ids, "out_ids", torch.int32, dev)
     if out_ids.shape != (T, K) or out_scores.shape != (T, K):
         raise ValueError("outputs must be (T, K)")
-    with torch.cuda.device(dev):
-        st = dcp_local_topk_ex(logits.data_ptr(), T, L, ld, K, rank, dcp,
-                               None if row_starts is None else row_starts.data_ptr(),
-                               _layout(layout), out_scores.data_ptr(), out_ids.data_ptr(),
-                               _stream_handle(stream))
+    st = _on_device(dev, lambda: library().dcp_local_topk_ex(
+        logits.data_ptr(), T, L, ld, K, rank, dcp,
+        None if row_starts is None else row_starts.data_ptr(),
+        _layout(layout), out_scores.data_ptr(), out_ids.data_ptr(),
+        _stream_handle(stream, dev)))
     if st != DCP_OK:
         raise DcpError(st, "dcp_local_topk_ex")
     return out_scores, out_ids
@@ -279,11 +297,11 @@ def fused_topk(logits, K, L=None, row_starts=None, out_scores=None, out_ids=None
     _check(out_ids, "out_ids", torch.int32, dev)
     if out_ids.shape != (T, K) or out_scores.shape != (T, K):
         raise ValueError("outputs must be (T, K)")
-    with torch.cuda.device(dev):
-        st = dcp_fused_topk_ex(logits.data_ptr(), T, dcp, L, ld, K,
-                               None if row_starts is None else row_starts.data_ptr(),
-                               _layout(layout), out_scores.data_ptr(), out_ids.data_ptr(),
-                               _stream_handle(stream))
+    st = _on_device(dev, lambda: library().dcp_fused_topk_ex(
+        logits.data_ptr(), T, dcp, L, ld, K,
+        None if row_starts is None else row_starts.data_ptr(),
+        _layout(layout), out_scores.data_ptr(), out_ids.data_ptr(),
+        _stream_handle(stream, dev)))
     if st != DCP_OK:
         raise DcpError(st, "dcp_fused_topk_ex")
     return out_scores, out_ids
