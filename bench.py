@@ -188,6 +188,19 @@ def median_of_reps(torch, fn, stream, reps=7, launches=200, graph=False):
     return statistics.median(out[1:])
 
 
+def replica_throughput(torch, local_ms, rows_per_step, steps, dist=None, device=None):
+    """Whole-job rows/s over the ranks of a replicas-only run: every rank
+    processed rows_per_step * steps rows; the job took the slowest rank's
+    time.  Returns (rows/s, max ms over ranks, world size)."""
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    world = 1
+    if dist is not None and dist.is_initialized():
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        world = dist.get_world_size()
+    max_ms = float(t.item())
+    return rows_per_step * steps * world / (max_ms / 1000.0), max_ms, world
+
+
 def cpu_oracle_sample(m, budget_s=10.0):
     """The oracle as it stands, single-threaded, on rows of the workload until
     about budget_s seconds have passed.  Returns (rows/s, rows, seconds)."""
@@ -304,11 +317,7 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
     per = durations(evs)
     total_ms = evs[0].elapsed_time(evs[-1])
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
-    value = m.T * args.steps * world / (max_ms / 1000.0)
+    value, max_ms, _ = replica_throughput(torch, total_ms, m.T, args.steps, dist, dev)
 
     # roofline of the merge kernel (the only kernel of the step)
     alg_bytes = m.algorithmic_bytes()
