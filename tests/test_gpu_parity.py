@@ -376,3 +376,60 @@ def test_interleaved_local_then_merge():
     torch.cuda.synchronize()
     want_s, want_i = oracle.fused_topk(logits, K, interleaved=True)
     assert_same((out_ids.cpu().numpy(), out_scores.cpu().numpy()), (want_i, want_s), "interleaved")
+
+
+def test_graph_captured_prefill_chunks():
+    """Prefill merges captured in CUDA graphs and replayed with new inputs
+    ("Reserve the sparse indexer's DCP top-k merge scratch through the
+    workspace manager", Purpose: the merge walks the rows in 1024-row chunks
+    and reserves its scratch up front; rows are independent):
+    * one call over T=3000 rows, whose kernel walks the chunks itself;
+    * one call per 1024-row chunk on chunk buffers, as a caller holding them
+      would make.
+    Sampled rows equal the oracle's, and the library asks for no workspace."""
+    T, dcp, K, chunk = 3000, 4, 2048, 1024
+    assert dk.dcp_topk_merge_workspace_size(T, dcp, K) == 0
+    m1 = workloads.prefill(seed=31, T=T)
+    m2 = workloads.prefill(seed=32, T=T)
+    rows = [0, 1, 1023, 1024, 1025, 2047, 2048, 2999]
+    want = oracle.merge(m2.scores, m2.ids, m2.row_starts, rows=rows)
+
+    # one call
+    s, i, rs = _dev(m1.scores), _dev(m1.ids), _dev(m1.row_starts)
+    out_ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    out_scores = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    dk.merge(s, i, rs, out_ids=out_ids, out_scores=out_scores)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dk.merge(s, i, rs, out_ids=out_ids, out_scores=out_scores)
+    s.copy_(_dev(m2.scores))
+    i.copy_(_dev(m2.ids))
+    rs.copy_(_dev(m2.row_starts))
+    g.replay()
+    torch.cuda.synchronize()
+    assert_same((out_ids.cpu().numpy()[rows], out_scores.cpu().numpy()[rows]), want, "one call")
+
+    # one call per chunk, on chunk buffers
+    bounds = [(c0, min(T, c0 + chunk)) for c0 in range(0, T, chunk)]
+    bufs = [(_dev(np.ascontiguousarray(m1.scores[:, a:b])), _dev(np.ascontiguousarray(m1.ids[:, a:b])),
+             _dev(m1.row_starts[a:b])) for a, b in bounds]
+    out_ids.zero_()
+    out_scores.zero_()
+
+    def chunks():
+        for (a, b), (cs, ci, cr) in zip(bounds, bufs):
+            dk.merge(cs, ci, cr, out_ids=out_ids[a:b], out_scores=out_scores[a:b])
+
+    chunks()
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2):
+        chunks()
+    for (a, b), (cs, ci, cr) in zip(bounds, bufs):
+        cs.copy_(_dev(np.ascontiguousarray(m2.scores[:, a:b])))
+        ci.copy_(_dev(np.ascontiguousarray(m2.ids[:, a:b])))
+        cr.copy_(_dev(m2.row_starts[a:b]))
+    g2.replay()
+    torch.cuda.synchronize()
+    assert_same((out_ids.cpu().numpy()[rows], out_scores.cpu().numpy()[rows]), want, "per chunk")
