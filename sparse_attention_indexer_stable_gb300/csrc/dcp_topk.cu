@@ -441,7 +441,11 @@ static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out
                               int32_t* out_ids, cudaStream_t stream) {
   DeviceInfo* d = nullptr;
   if (device_info(&d) != cudaSuccess) return DCP_ERR_CUDA;
-  const size_t smem = stream_smem_bytes(src.score_words(), src.ids_words());
+  // one 1024-thread CTA per row (few rows, or up to 16384 candidates per row),
+  // else two 512-thread CTAs per SM walking the rows
+  const bool one_per_sm = T <= d->sms || n > kStreamMaxN;
+  const size_t smem = one_per_sm ? stream_smem_bytes<1024>(src.score_words(), src.ids_words())
+                                 : stream_smem_bytes<512>(src.score_words(), src.ids_words());
   const bool stream_ok =
       src.vec4 && K <= kStreamMaxK && smem <= (size_t)d->max_smem_optin && n <= kStreamMaxNWide;
   cudaError_t e;

@@ -9,8 +9,9 @@
 // selection and final order come out of one two-level bucket pass instead of
 // a radix select followed by a sort:
 //
-//  L1      an 11-bit histogram of the score keys' top bits over every
-//          candidate (the "radix pass over 32-bit score keys first" of
+//  L1      a 12-bit (11-bit in 1024-thread CTAs) histogram of the score
+//          keys' top bits over every candidate (the "radix pass over 32-bit
+//          score keys first" of
 //          "[Kernel] Optimize CuTeDSL DCP top-k merge", Summary) locates the
 //          bin b1 holding the K-th largest key; bins above b1 are all winners.
 //  COMPACT the candidates of bins >= b1 ("live", about K of them) are packed
@@ -50,24 +51,48 @@ namespace dcp {
 constexpr int kStreamMaxN = 8192;             // candidates per row (two CTAs per SM)
 constexpr int kStreamMaxNWide = 16384;        // candidates per row (one CTA per SM)
 constexpr int kStreamMaxK = 2048;
-constexpr int kLiveMax = 3072;                // live candidates per row
-constexpr int kFineMax = kStreamMaxK + 1024;  // fine buckets per row (bound, see SCAN1)
 constexpr uint32_t kBigBucket = 255;          // a larger bucket starting before K sends the row to the fallback
 constexpr int kRankMax = kStreamMaxK + 256;   // list positions up to the end of the bucket straddling K
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr unsigned long long kStageWaitLimit = 1ull << 31;  // cycles (about 1 s) to wait for a row's copy
 constexpr uint32_t kStatusCopyTimeout = 1u;     // device status bit: a staging copy timed out
 
+// Per-row sizes for a CTA of NT threads.
+// - The 512-thread CTAs walk many rows two to an SM: their L1 bins are the
+//   score keys' top 12 bits, which keeps the live set near K even for
+//   bf16-valued scores, and their shared memory is tighter: a live list of
+//   2560 keys (a fuller threshold bin is refined first) and 2560 fine buckets
+//   (at most 512 per L1 bin).
+// - The 1024-thread CTAs (one row each, or rows of up to 16384 candidates)
+//   use 11-bit bins, 3072 live keys and 3072 fine buckets (at most 1024 per
+//   bin): a smaller histogram to scan and reset per row.
+// Capacities are multiples of NT.
+template <int NT>
+struct StreamCaps {
+  static constexpr int kL1Bits = NT == 512 ? 12 : 11;
+  static constexpr int kL1Shift = 32 - kL1Bits;
+  static constexpr int kL1Bins = 1 << kL1Bits;
+  static constexpr uint32_t kLowMask = (1u << kL1Shift) - 1u;  // key bits below the L1 bin
+  static constexpr int kRefShift = kL1Shift - 11;  // the refinement digit: 11 bits below the bin
+  static constexpr uint32_t kPadBin = 0x007FFFFFu >> kL1Shift;  // bin of -inf keys (padding)
+  static constexpr int kLive = NT == 512 ? 2560 : 3072;
+  static constexpr int kFine = NT == 512 ? 2560 : 3072;
+  // fine buckets per L1 bin; the bins above b1 hold fewer than K keys and
+  // get fewer than K buckets, so a row needs fewer than kFine
+  static constexpr uint32_t kBinBuckets = (uint32_t)(kFine - kStreamMaxK);
+};
+
+template <int LIVE, int FINE, int BINS>
 struct StreamShared {
-  unsigned long long live[kLiveMax];  // live keys; then in bucket order; fallback: sorted winners
-  uint32_t fine[kFineMax];            // L2 sizes, then start << 16 | fill cursor
+  unsigned long long live[LIVE];      // live keys; then in bucket order; fallback: sorted winners
+  uint32_t fine[FINE];                // L2 sizes, then start << 16 | fill cursor
   union {
-    uint32_t table[kHistBins];        // L1 counts, then first bucket << 8 | log2(buckets)
+    uint32_t table[BINS];             // L1 counts, then first bucket << 8 | log2(buckets)
     SelectShared sel;                 // the fallback's radix-select state
   } u;
   uint32_t wa[kMaxWarps];
   uint32_t wb[kMaxWarps];
-  uint32_t stat_or[2];                // OR of the raw scores' low 21 bits; OR of ~ids (not 0)
+  uint32_t stat_or[2];                // OR of the raw scores' bits below the bin; OR of ~ids (not 0)
   uint32_t stat_and[2];               // [1]: AND of ~ids (not 0)
   uint32_t live_cursor;
   uint32_t b1;                        // L1 bin of the K-th largest key
@@ -80,16 +105,26 @@ struct StreamShared {
   unsigned long long stage_bar;       // completes when a row's scores land in the stage
   unsigned long long ids_bar;         // completes when a row's ids land in the aux region
 };
+template <int NT>
+using StreamSharedFor =
+    StreamShared<StreamCaps<NT>::kLive, StreamCaps<NT>::kFine, StreamCaps<NT>::kL1Bins>;
+
 // 16-byte vector accesses to these arrays need 16-byte aligned offsets.
-static_assert(offsetof(StreamShared, live) % 16 == 0, "live must be 16-byte aligned");
-static_assert(offsetof(StreamShared, fine) % 16 == 0, "fine must be 16-byte aligned");
-static_assert(offsetof(StreamShared, u) == offsetof(StreamShared, fine) + sizeof(uint32_t) * kFineMax,
-              "the table must follow fine directly (one region to reset)");
+template <class S, int FINE>
+constexpr bool stream_layout_ok() {
+  return offsetof(S, live) % 16 == 0 && offsetof(S, fine) % 16 == 0 &&
+         offsetof(S, u) == offsetof(S, fine) + sizeof(uint32_t) * FINE &&  // one region to reset
+         offsetof(S, stage_bar) % 8 == 0;
+}
+static_assert(stream_layout_ok<StreamSharedFor<512>, StreamCaps<512>::kFine>(), "layout");
+static_assert(stream_layout_ok<StreamSharedFor<1024>, StreamCaps<1024>::kFine>(), "layout");
+static_assert(StreamCaps<512>::kLive % 512 == 0 && StreamCaps<512>::kFine % 512 == 0, "caps");
+static_assert(StreamCaps<1024>::kLive % 1024 == 0 && StreamCaps<1024>::kFine % 1024 == 0, "caps");
+static_assert(StreamCaps<512>::kFine >= 2048 && StreamCaps<512>::kLive >= kStreamMaxK, "caps");
 static_assert(kRankMax >= kStreamMaxK + (int)kBigBucket - 1, "list positions must reach the straddling bucket's end");
 // Scratch for RANK in the aux region: rank keys (u64) then bucket info (u16)
 // per list position.
 constexpr int kScratchWords = (kRankMax * 8 + kRankMax * 2 + 15) / 16 * 4;
-static_assert(offsetof(StreamShared, stage_bar) % 8 == 0, "mbarrier must be 8-byte aligned");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -152,18 +187,28 @@ __device__ __forceinline__ void grid_dependency_wait() {
 }
 
 // Fine buckets for an L1 bin of h candidates: half of h rounded up to a power
-// of two, at least 1 and at most 1024 (0 for an empty bin).  Never more than
-// h, so the bins above b1 (fewer than K candidates) get fewer than K buckets.
-__device__ __forceinline__ uint32_t fine_buckets(uint32_t h) {
+// of two, at least 1 and at most cap (a power of two; 0 for an empty bin).
+// Never more than h, so the bins above b1 (fewer than K candidates) get fewer
+// than K buckets.
+__device__ __forceinline__ uint32_t fine_buckets(uint32_t h, uint32_t cap) {
   const uint32_t p = (1u << (32 - __clz(h - 1u))) >> 1;  // next power of two >= h, halved
-  return h == 0u ? 0u : min(max(p, 1u), 1024u);
+  return h == 0u ? 0u : min(max(p, 1u), cap);
 }
 
 // Loads P consecutive histogram words at p (ascending bins) into h in
 // descending bin order.
 template <int P>
 __device__ __forceinline__ void load_bins_desc(const uint32_t* p, uint32_t (&h)[P]) {
-  if constexpr (P == 4) {
+  if constexpr (P % 4 == 0 && P > 4) {
+#pragma unroll
+    for (int g = 0; g < P / 4; ++g) {
+      const uint4 w = *reinterpret_cast<const uint4*>(p + 4 * g);
+      h[P - 1 - 4 * g] = w.x;
+      h[P - 2 - 4 * g] = w.y;
+      h[P - 3 - 4 * g] = w.z;
+      h[P - 4 - 4 * g] = w.w;
+    }
+  } else if constexpr (P == 4) {
     const uint4 w = *reinterpret_cast<const uint4*>(p);
     h[0] = w.w;
     h[1] = w.z;
@@ -214,13 +259,15 @@ __device__ __forceinline__ void find_digit_desc(const uint32_t* hist, uint32_t n
   }
 }
 
-// Shared-memory bytes of the streaming kernel: the state, the stage for a
-// row's `score_words` scores, and the aux region (the row's `ids_words` ids
-// when they are staged, RANK's scratch after COMPACT; the larger of the two).
+// Shared-memory bytes of the streaming kernel with NT threads: the state, the
+// stage for a row's `score_words` scores, and the aux region (the row's
+// `ids_words` ids when they are staged, RANK's scratch after COMPACT; the
+// larger of the two).
+template <int NT>
 inline size_t stream_smem_bytes(int score_words, int ids_words) {
   const int aux = ids_words > kScratchWords ? ids_words : kScratchWords;
-  return ((sizeof(StreamShared) + 15) & ~(size_t)15) + (size_t)((score_words + 3) & ~3) * 4 +
-         (size_t)((aux + 3) & ~3) * 4;
+  return ((sizeof(StreamSharedFor<NT>) + 15) & ~(size_t)15) +
+         (size_t)((score_words + 3) & ~3) * 4 + (size_t)((aux + 3) & ~3) * 4;
 }
 
 // Orders this thread's earlier shared-memory writes before later bulk copies
@@ -243,14 +290,23 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   constexpr int kWarpsT = NT / 32;
   constexpr int kVec = MAXN / 4 / NT;  // 16-byte score chunks per thread
   constexpr int kItems = 4 * kVec;
+  using Caps = StreamCaps<NT>;
+  using Shared = StreamSharedFor<NT>;
+  constexpr int kLiveMax = Caps::kLive;
+  constexpr int kFineMax = Caps::kFine;
+  constexpr int kL1Bins = Caps::kL1Bins;
+  constexpr int kL1Shift = Caps::kL1Shift;
+  constexpr uint32_t kLowMask = Caps::kLowMask;
+  constexpr int kRefShift = Caps::kRefShift;
+  constexpr uint32_t kPadBin = Caps::kPadBin;
   constexpr int kLivePer = kLiveMax / NT;
   constexpr int kFinePer = kFineMax / NT;
-  constexpr int kBinsPer = kHistBins / NT;
+  constexpr int kBinsPer = kL1Bins / NT;
 
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  StreamShared& s = *reinterpret_cast<StreamShared*>(smem_raw);
+  Shared& s = *reinterpret_cast<Shared*>(smem_raw);
   uint32_t* stage =
-      reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(StreamShared) + 15) & ~(size_t)15));
+      reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(Shared) + 15) & ~(size_t)15));
   const int n = src.count();  // multiple of 4, <= MAXN
   uint32_t* aux = stage + n;  // the row's ids (when staged), then RANK's scratch
   unsigned long long* rkl = reinterpret_cast<unsigned long long*>(aux);
@@ -262,7 +318,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
 
   // Shared-memory set-up first: it touches no global memory, so it may run
   // while the stream's previous kernel is still finishing.
-  zero_words<NT>(s.fine, kFineMax + kHistBins);  // fine and the table behind it
+  zero_words<NT>(s.fine, kFineMax + kL1Bins);  // fine and the table behind it
   if (tid == 0) {
     s.live_cursor = 0u;
     s.p_end = 0u;
@@ -305,8 +361,8 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     // row's are consumed (after L1); its ids follow at the end of the row (the
     // aux region serves RANK until then) and are needed only by COMPACT.
 
-    // ---- L1: histogram of the score keys' top 11 bits ---------------------
-    // Also ORs the low 21 bits of every raw score: the bits that are zero in
+    // ---- L1: histogram of the score keys' top bits -------------------------
+    // Also ORs the raw scores' bits below the bin: the bits that are zero in
     // all of them are constant in every key of one sign (bf16-valued scores
     // leave the low 16 zero), which the buckets below skip.
     uint32_t keys[kItems];
@@ -322,13 +378,13 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         keys[4 * v + 2] = score_key(w.z);
         keys[4 * v + 3] = score_key(w.w);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) atomicAdd(&s.u.table[keys[4 * v + e] >> 21], 1u);
+        for (int e = 0; e < 4; ++e) atomicAdd(&s.u.table[keys[4 * v + e] >> kL1Shift], 1u);
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) keys[4 * v + e] = 0u;
       }
     }
-    raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & 0x1FFFFFu);
+    raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & kLowMask);
     if (lane == 0 && raw_or) atomicOr(&s.stat_or[0], raw_or);
     __syncthreads();
     // L1 was the last reader of the staged scores (the rest of the row works
@@ -342,7 +398,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     // band of bins) only reports a zero total.
     {
       uint32_t h[kBinsPer], f[kBinsPer];
-      load_bins_desc<kBinsPer>(s.u.table + kHistBins - kBinsPer * (tid + 1), h);
+      load_bins_desc<kBinsPer>(s.u.table + kL1Bins - kBinsPer * (tid + 1), h);
       uint32_t any = 0u;
 #pragma unroll
       for (int e = 0; e < kBinsPer; ++e) any |= h[e];
@@ -351,7 +407,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       if (warp_busy) {
 #pragma unroll
         for (int e = 0; e < kBinsPer; ++e) {
-          f[e] = fine_buckets(h[e]);
+          f[e] = fine_buckets(h[e], Caps::kBinBuckets);
           local += (f[e] << 16) | h[e];
         }
         incl = warp_inclusive_scan(local);
@@ -366,7 +422,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
 #pragma unroll
         for (int e = 0; e < kBinsPer; ++e) {
           const uint32_t above = ex & 0xFFFFu, fabove = ex >> 16;
-          const int b = kHistBins - 1 - (kBinsPer * tid + e);
+          const int b = kL1Bins - 1 - (kBinsPer * tid + e);
           if (h[e] != 0u) {
             if (above < (uint32_t)ksel && (uint32_t)ksel <= above + h[e]) {
               s.b1 = (uint32_t)b;
@@ -396,7 +452,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
 
     const uint32_t b1 = s.b1;
     const int nfine = (int)s.nfine;
-    // Live candidates are those with (key >> 10) >= live_from.  Normally that
+    // Live candidates are those with (key >> kRefShift) >= live_from.  Normally that
     // is every candidate of bins >= b1; when bin b1 alone is too full for the
     // live list, its next 11 key bits are histogrammed (in `fine`, still
     // zero) and only its candidates from the digit holding the K-th key on
@@ -405,8 +461,8 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     if (s.nlive > (uint32_t)kLiveMax) {
 #pragma unroll
       for (int j = 0; j < kItems; ++j) {
-        if ((tid + (j >> 2) * NT) < n4 && (keys[j] >> 21) == b1)
-          atomicAdd(&s.fine[(keys[j] >> 10) & 0x7FFu], 1u);
+        if ((tid + (j >> 2) * NT) < n4 && (keys[j] >> kL1Shift) == b1)
+          atomicAdd(&s.fine[(keys[j] >> kRefShift) & 0x7FFu], 1u);
       }
       __syncthreads();
       find_digit_desc<NT>(s.fine, (uint32_t)ksel - s.above_b1, s.wa, s.wb, s.found_digit,
@@ -414,7 +470,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       __syncthreads();
       live_from |= s.found_digit;
       const uint32_t nl = s.above_b1 + s.found_above + s.found_count;
-      zero_words<NT>(s.fine, kHistBins);
+      zero_words<NT>(s.fine, kHistBins);  // the refinement histogram: 2048 words of fine
       __syncthreads();
       if (tid == 0) s.nlive = nl;
       __syncthreads();
@@ -425,7 +481,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     // ---- COMPACT: live candidates into a dense list -------------------------
     if (fast) {
       uint32_t mask = 0u;
-      const uint32_t lf = live_from << 10;  // live: key >= lf
+      const uint32_t lf = live_from << kRefShift;  // live: key >= lf
       if (lf != 0u) {
         // candidates past the row hold key 0 (< lf)
 #pragma unroll
@@ -470,18 +526,18 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     unsigned long long lkey[kLivePer];
     uint32_t gslot[kLivePer];
     if (fast) {
-      // For finite scores the low 21 key bits below tzf are equal within a
-      // sign, and the bits of ~id at or above ibf are equal for every live
-      // candidate (but padding), so within one bin keys are ordered like
-      // y = (low key bits >> tzf) << ibf | (~id low ibf bits), a wf-bit number
-      // whose top q bits name the bucket.  Bins 0..3 (-inf, where padding
-      // lives, and below) keep every bit (53).
+      // For finite scores the key bits below the L1 bin and below tzf are
+      // equal within a sign, and the bits of ~id at or above ibf are equal for
+      // every live candidate (but padding), so within one bin keys are
+      // ordered like y = (low key bits >> tzf) << ibf | (~id low ibf bits), a
+      // wf-bit number whose top q bits name the bucket.  Bins up to kPadBin
+      // (-inf, where padding lives, and below) keep every bit.
       const uint32_t ro = s.stat_or[0];
       const uint32_t vi = s.stat_or[1] ^ s.stat_and[1];
-      const int tzf = ro ? min(__ffs(ro) - 1, 21) : 21;
+      const int tzf = ro ? min(__ffs(ro) - 1, kL1Shift) : kL1Shift;
       const int ibf = vi ? 32 - __clz(vi) : 0;
       const uint32_t imask = ibf >= 32 ? 0xFFFFFFFFu : ((1u << ibf) - 1u);
-      const int wf = 21 - tzf + ibf;
+      const int wf = kL1Shift - tzf + ibf;
 #pragma unroll
       for (int u = 0; u < kLivePer; ++u) {
         const int e = tid + u * NT;
@@ -491,17 +547,17 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
           lkey[u] = s.live[e];
           const uint32_t k = (uint32_t)(lkey[u] >> 32);
           const uint32_t inv = (uint32_t)lkey[u];
-          const uint32_t bin = k >> 21;
+          const uint32_t bin = k >> kL1Shift;
           const uint32_t tb = s.u.table[bin];
           const int q = (int)(tb & 0xFFu);
           unsigned long long y;
           int w;
-          if (bin > 3u) {
-            y = ((unsigned long long)((k & 0x1FFFFFu) >> tzf) << ibf) | (inv & imask);
+          if (bin > kPadBin) {
+            y = ((unsigned long long)((k & kLowMask) >> tzf) << ibf) | (inv & imask);
             w = wf;
           } else {
-            y = ((unsigned long long)(k & 0x1FFFFFu) << 32) | inv;
-            w = 53;
+            y = ((unsigned long long)(k & kLowMask) << 32) | inv;
+            w = kL1Shift + 32;
           }
           const uint32_t sub = w >= q ? (uint32_t)(y >> (w - q)) : (uint32_t)(y << (q - w));
           const uint32_t g = (tb >> 8) + ((1u << q) - 1u - sub);
@@ -578,8 +634,9 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       // Per list position the aux region records the bucket's size << 8 | the
       // slot and, for shared buckets, rank_key(key, slot) =
       // key << 11 | (255 - slot): members of a bucket share their key's top
-      // 11 bits (the L1 bin), so this is the key order within the bucket,
-      // identical keys told apart by their slot (the smaller slot first).
+      // 11 or 12 bits (the L1 bin), so dropping 11 of them keeps the key order
+      // within the bucket, identical keys told apart by their slot (the
+      // smaller slot first).
 #pragma unroll
       for (int u = 0; u < kLivePer; ++u) {
         if (gslot[u] != kNone) {
@@ -657,7 +714,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     if constexpr (Source::kStagesIds)
       if (tid == 0 && t + G < T) src.issue_ids(t + G, aux, &s.ids_bar);
 
-    zero_words<NT>(s.fine, kFineMax + kHistBins);  // fine and the table behind it
+    zero_words<NT>(s.fine, kFineMax + kL1Bins);  // fine and the table behind it
     if (tid == 0) {
       s.live_cursor = 0u;
       s.p_end = 0u;
