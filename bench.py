@@ -414,6 +414,19 @@ def decode_and_sweep(torch, dk, dev, stream):
             "us_per_launch": median_of_reps(torch, raw, stream),
             "us_per_graph_replay": median_of_reps(torch, raw, stream, graph=True)}
     out["selector_shapes_K2048"] = shapes
+    # K=4096 (16 rows, dcp=4: 16384 candidates per row)
+    m = workloads.decode(seed=77, T=16, dcp=4, K=4096)
+    s4 = torch.from_numpy(m.scores).to(dev)
+    i4 = torch.from_numpy(m.ids).to(dev)
+    oi4 = torch.empty((m.T, m.K), dtype=torch.int32, device=dev)
+    os4 = torch.empty((m.T, m.K), dtype=torch.float32, device=dev)
+    args4 = (s4.data_ptr(), i4.data_ptr(), m.T, m.dcp, m.K, None, oi4.data_ptr(), os4.data_ptr(),
+             None, 0, stream.cuda_stream)
+
+    def raw4():
+        dk.library().dcp_topk_merge(*args4)
+
+    out["merge_T16_dcp4_K4096_us_per_launch"] = median_of_reps(torch, raw4, stream)
     sweep = {}
     K = 2048
     for T in workloads.SWEEP_T:

@@ -342,6 +342,24 @@ static cudaError_t allow_max_smem(K kernel, int bytes) {
                               (int)cudaSharedmemCarveoutMaxShared);
 }
 
+// The streaming kernel's instantiations for one source: 512-thread CTAs two
+// per SM, 1024-thread CTAs one per row, 1024-thread CTAs for rows of up to
+// 16384 candidates, and the same for K up to 4096.
+template <class Source>
+static cudaError_t allow_stream_kernels(int smem) {
+  cudaError_t e;
+  if ((e = allow_max_smem(topk_stream_kernel<512, kStreamMaxN, kStreamMaxK, Source>, smem)) !=
+      cudaSuccess)
+    return e;
+  if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxN, kStreamMaxK, Source>, smem)) !=
+      cudaSuccess)
+    return e;
+  if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxK, Source>,
+                          smem)) != cudaSuccess)
+    return e;
+  return allow_max_smem(topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxKWide, Source>, smem);
+}
+
 // Per-device launch limits and kernel attributes, set once per device (the
 // first call on a device must therefore not be inside a stream capture).
 static cudaError_t device_info(DeviceInfo** out) {
@@ -364,30 +382,9 @@ static cudaError_t device_info(DeviceInfo** out) {
     if ((e = allow_max_smem(topk_rows_kernel<MergeSource>, smem)) != cudaSuccess) return e;
     if ((e = allow_max_smem(topk_rows_kernel<LocalSource>, smem)) != cudaSuccess) return e;
     if ((e = allow_max_smem(topk_rows_kernel<FusedSource>, smem)) != cudaSuccess) return e;
-    if ((e = allow_max_smem(topk_stream_kernel<512, kStreamMaxN, MergeSource>, smem)) != cudaSuccess)
-      return e;
-    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxN, MergeSource>, smem)) !=
-        cudaSuccess)
-      return e;
-    if ((e = allow_max_smem(topk_stream_kernel<512, kStreamMaxN, LocalSource>, smem)) != cudaSuccess)
-      return e;
-    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxN, LocalSource>, smem)) !=
-        cudaSuccess)
-      return e;
-    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxNWide, FusedSource>, smem)) !=
-        cudaSuccess)
-      return e;
-    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxNWide, MergeSource>, smem)) !=
-        cudaSuccess)
-      return e;
-    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxNWide, LocalSource>, smem)) !=
-        cudaSuccess)
-      return e;
-    if ((e = allow_max_smem(topk_stream_kernel<512, kStreamMaxN, FusedSource>, smem)) != cudaSuccess)
-      return e;
-    if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxN, FusedSource>, smem)) !=
-        cudaSuccess)
-      return e;
+    if ((e = allow_stream_kernels<MergeSource>(smem)) != cudaSuccess) return e;
+    if ((e = allow_stream_kernels<LocalSource>(smem)) != cudaSuccess) return e;
+    if ((e = allow_stream_kernels<FusedSource>(smem)) != cudaSuccess) return e;
     if ((e = status_word(&d.status)) != cudaSuccess) return e;
     d.configured.store(true, std::memory_order_release);
   }
@@ -441,28 +438,33 @@ static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out
                               int32_t* out_ids, cudaStream_t stream) {
   DeviceInfo* d = nullptr;
   if (device_info(&d) != cudaSuccess) return DCP_ERR_CUDA;
-  // one 1024-thread CTA per row (few rows, or up to 16384 candidates per row),
-  // else two 512-thread CTAs per SM walking the rows
-  const bool one_per_sm = T <= d->sms || n > kStreamMaxN;
-  const size_t smem = one_per_sm ? stream_smem_bytes<1024>(src.score_words(), src.ids_words())
-                                 : stream_smem_bytes<512>(src.score_words(), src.ids_words());
-  const bool stream_ok =
-      src.vec4 && K <= kStreamMaxK && smem <= (size_t)d->max_smem_optin && n <= kStreamMaxNWide;
+  // The streaming kernel when 16-byte copies are possible and the row fits
+  // it: two 512-thread CTAs per SM walking many rows of up to 8192
+  // candidates; else one 1024-thread CTA per row (few rows, up to 16384
+  // candidates, or K up to 4096).
+  const bool big_k = K > kStreamMaxK;
+  const bool two_per_sm = T > d->sms && n <= kStreamMaxN && !big_k;
+  const size_t smem =
+      big_k ? stream_smem_bytes<1024, kStreamMaxKWide>(src.score_words(), src.ids_words())
+      : two_per_sm ? stream_smem_bytes<512>(src.score_words(), src.ids_words())
+                   : stream_smem_bytes<1024>(src.score_words(), src.ids_words());
+  const bool stream_ok = src.vec4 && K <= kStreamMaxKWide && n <= kStreamMaxNWide &&
+                         smem <= (size_t)d->max_smem_optin;
+  const int grid1 = T < d->sms ? T : d->sms;
   cudaError_t e;
-  if (stream_ok && n > kStreamMaxN) {
-    // up to 16384 candidates per row: one 1024-thread CTA per SM
-    const int grid = T < d->sms ? T : d->sms;
-    e = launch_serialized(topk_stream_kernel<1024, kStreamMaxNWide, Source>, grid, 1024, smem,
-                          stream, src, T, K, out_scores, out_ids, d->status);
+  if (stream_ok && big_k) {
+    e = launch_serialized(topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxKWide, Source>,
+                          grid1, 1024, smem, stream, src, T, K, out_scores, out_ids, d->status);
+  } else if (stream_ok && n > kStreamMaxN) {
+    e = launch_serialized(topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxK, Source>, grid1,
+                          1024, smem, stream, src, T, K, out_scores, out_ids, d->status);
+  } else if (stream_ok && !two_per_sm) {
+    e = launch_serialized(topk_stream_kernel<1024, kStreamMaxN, kStreamMaxK, Source>, grid1, 1024,
+                          smem, stream, src, T, K, out_scores, out_ids, d->status);
   } else if (stream_ok) {
-    if (T <= d->sms) {
-      e = launch_serialized(topk_stream_kernel<1024, kStreamMaxN, Source>, T, 1024, smem, stream,
-                            src, T, K, out_scores, out_ids, d->status);
-    } else {
-      const int grid = T < 2 * d->sms ? T : 2 * d->sms;
-      e = launch_serialized(topk_stream_kernel<512, kStreamMaxN, Source>, grid, 512, smem, stream,
-                            src, T, K, out_scores, out_ids, d->status);
-    }
+    const int grid = T < 2 * d->sms ? T : 2 * d->sms;
+    e = launch_serialized(topk_stream_kernel<512, kStreamMaxN, kStreamMaxK, Source>, grid, 512,
+                          smem, stream, src, T, K, out_scores, out_ids, d->status);
   } else {
     const size_t gsmem = row_smem_bytes(n, K);
     if (gsmem > (size_t)d->max_smem_optin) return DCP_ERR_UNSUPPORTED;

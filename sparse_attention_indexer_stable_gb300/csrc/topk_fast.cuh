@@ -1,6 +1,6 @@
-// topk_fast.cuh -- the streaming top-K path for rows of up to 8192 candidates
-// and K <= 2048 (the merge at DCP=4, K=2048 and the local top-K over 4096
-// columns fall here).
+// topk_fast.cuh -- the streaming top-K path for rows of up to 16384
+// candidates and K <= 4096 (the merge at DCP=4, K=2048, the local top-K over
+// 4096 columns and the fused top-K over all shards fall here).
 //
 // A persistent grid walks the rows: CTAs of 512 threads, two per SM, for many
 // rows (one CTA's row streams in from HBM while the other CTA selects), or one
@@ -50,24 +50,24 @@ namespace dcp {
 
 constexpr int kStreamMaxN = 8192;             // candidates per row (two CTAs per SM)
 constexpr int kStreamMaxNWide = 16384;        // candidates per row (one CTA per SM)
-constexpr int kStreamMaxK = 2048;
+constexpr int kStreamMaxK = 2048;             // K of the regular instantiations
+constexpr int kStreamMaxKWide = 4096;         // K of the one-CTA-per-row instantiation for larger K
 constexpr uint32_t kBigBucket = 255;          // a larger bucket starting before K sends the row to the fallback
-constexpr int kRankMax = kStreamMaxK + 256;   // list positions up to the end of the bucket straddling K
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr unsigned long long kStageWaitLimit = 1ull << 31;  // cycles (about 1 s) to wait for a row's copy
 constexpr uint32_t kStatusCopyTimeout = 1u;     // device status bit: a staging copy timed out
 
-// Per-row sizes for a CTA of NT threads.
+// Per-row sizes for a CTA of NT threads selecting up to KMAX winners.
 // - The 512-thread CTAs walk many rows two to an SM: their L1 bins are the
 //   score keys' top 12 bits, which keeps the live set near K even for
 //   bf16-valued scores, and their shared memory is tighter: a live list of
 //   2560 keys (a fuller threshold bin is refined first) and 2560 fine buckets
 //   (at most 512 per L1 bin).
 // - The 1024-thread CTAs (one row each, or rows of up to 16384 candidates)
-//   use 11-bit bins, 3072 live keys and 3072 fine buckets (at most 1024 per
-//   bin): a smaller histogram to scan and reset per row.
+//   use 11-bit bins, KMAX + 1024 live keys and as many fine buckets (at most
+//   1024 per bin): a smaller histogram to scan and reset per row.
 // Capacities are multiples of NT.
-template <int NT>
+template <int NT, int KMAX = kStreamMaxK>
 struct StreamCaps {
   static constexpr int kL1Bits = NT == 512 ? 12 : 11;
   static constexpr int kL1Shift = 32 - kL1Bits;
@@ -75,11 +75,16 @@ struct StreamCaps {
   static constexpr uint32_t kLowMask = (1u << kL1Shift) - 1u;  // key bits below the L1 bin
   static constexpr int kRefShift = kL1Shift - 11;  // the refinement digit: 11 bits below the bin
   static constexpr uint32_t kPadBin = 0x007FFFFFu >> kL1Shift;  // bin of -inf keys (padding)
-  static constexpr int kLive = NT == 512 ? 2560 : 3072;
-  static constexpr int kFine = NT == 512 ? 2560 : 3072;
+  static constexpr int kLive = NT == 512 ? 2560 : KMAX + 1024;
+  static constexpr int kFine = NT == 512 ? 2560 : KMAX + 1024;
   // fine buckets per L1 bin; the bins above b1 hold fewer than K keys and
   // get fewer than K buckets, so a row needs fewer than kFine
-  static constexpr uint32_t kBinBuckets = (uint32_t)(kFine - kStreamMaxK);
+  static constexpr uint32_t kBinBuckets = (uint32_t)(kFine - KMAX);
+  // list positions: up to the end of the bucket straddling K
+  static constexpr int kRankMax = KMAX + 256;
+  // RANK's scratch in the aux region: rank keys (u64) then bucket info (u16)
+  // per list position
+  static constexpr int kScratchWords = (kRankMax * 8 + kRankMax * 2 + 15) / 16 * 4;
 };
 
 template <int LIVE, int FINE, int BINS>
@@ -105,9 +110,9 @@ struct StreamShared {
   unsigned long long stage_bar;       // completes when a row's scores land in the stage
   unsigned long long ids_bar;         // completes when a row's ids land in the aux region
 };
-template <int NT>
-using StreamSharedFor =
-    StreamShared<StreamCaps<NT>::kLive, StreamCaps<NT>::kFine, StreamCaps<NT>::kL1Bins>;
+template <int NT, int KMAX = kStreamMaxK>
+using StreamSharedFor = StreamShared<StreamCaps<NT, KMAX>::kLive, StreamCaps<NT, KMAX>::kFine,
+                                     StreamCaps<NT, KMAX>::kL1Bins>;
 
 // 16-byte vector accesses to these arrays need 16-byte aligned offsets.
 template <class S, int FINE>
@@ -116,15 +121,16 @@ constexpr bool stream_layout_ok() {
          offsetof(S, u) == offsetof(S, fine) + sizeof(uint32_t) * FINE &&  // one region to reset
          offsetof(S, stage_bar) % 8 == 0;
 }
-static_assert(stream_layout_ok<StreamSharedFor<512>, StreamCaps<512>::kFine>(), "layout");
-static_assert(stream_layout_ok<StreamSharedFor<1024>, StreamCaps<1024>::kFine>(), "layout");
-static_assert(StreamCaps<512>::kLive % 512 == 0 && StreamCaps<512>::kFine % 512 == 0, "caps");
-static_assert(StreamCaps<1024>::kLive % 1024 == 0 && StreamCaps<1024>::kFine % 1024 == 0, "caps");
-static_assert(StreamCaps<512>::kFine >= 2048 && StreamCaps<512>::kLive >= kStreamMaxK, "caps");
-static_assert(kRankMax >= kStreamMaxK + (int)kBigBucket - 1, "list positions must reach the straddling bucket's end");
-// Scratch for RANK in the aux region: rank keys (u64) then bucket info (u16)
-// per list position.
-constexpr int kScratchWords = (kRankMax * 8 + kRankMax * 2 + 15) / 16 * 4;
+template <int NT, int KMAX>
+constexpr bool stream_caps_ok() {
+  using C = StreamCaps<NT, KMAX>;
+  return stream_layout_ok<StreamSharedFor<NT, KMAX>, C::kFine>() && C::kLive % NT == 0 &&
+         C::kFine % NT == 0 && C::kFine >= 2048 /* the refinement histogram */ &&
+         C::kLive >= KMAX && C::kRankMax >= KMAX + (int)kBigBucket - 1;
+}
+static_assert(stream_caps_ok<512, kStreamMaxK>(), "caps");
+static_assert(stream_caps_ok<1024, kStreamMaxK>(), "caps");
+static_assert(stream_caps_ok<1024, kStreamMaxKWide>(), "caps");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -263,10 +269,11 @@ __device__ __forceinline__ void find_digit_desc(const uint32_t* hist, uint32_t n
 // stage for a row's `score_words` scores, and the aux region (the row's
 // `ids_words` ids when they are staged, RANK's scratch after COMPACT; the
 // larger of the two).
-template <int NT>
+template <int NT, int KMAX = kStreamMaxK>
 inline size_t stream_smem_bytes(int score_words, int ids_words) {
-  const int aux = ids_words > kScratchWords ? ids_words : kScratchWords;
-  return ((sizeof(StreamSharedFor<NT>) + 15) & ~(size_t)15) +
+  constexpr int kScratch = StreamCaps<NT, KMAX>::kScratchWords;
+  const int aux = ids_words > kScratch ? ids_words : kScratch;
+  return ((sizeof(StreamSharedFor<NT, KMAX>) + 15) & ~(size_t)15) +
          (size_t)((score_words + 3) & ~3) * 4 + (size_t)((aux + 3) & ~3) * 4;
 }
 
@@ -283,15 +290,16 @@ __device__ __forceinline__ void zero_words(uint32_t* p, int words) {
     *reinterpret_cast<uint4*>(p + i) = make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <int NT, int MAXN, class Source>
+template <int NT, int MAXN, int KMAX, class Source>
 __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     topk_stream_kernel(Source src, int T, int K, float* __restrict__ out_scores,
                        int32_t* __restrict__ out_ids, unsigned int* __restrict__ status) {
   constexpr int kWarpsT = NT / 32;
   constexpr int kVec = MAXN / 4 / NT;  // 16-byte score chunks per thread
   constexpr int kItems = 4 * kVec;
-  using Caps = StreamCaps<NT>;
-  using Shared = StreamSharedFor<NT>;
+  using Caps = StreamCaps<NT, KMAX>;
+  using Shared = StreamSharedFor<NT, KMAX>;
+  constexpr int kRankMax = Caps::kRankMax;
   constexpr int kLiveMax = Caps::kLive;
   constexpr int kFineMax = Caps::kFine;
   constexpr int kL1Bins = Caps::kL1Bins;

@@ -108,6 +108,13 @@ CASES = [
     (4, 4, 2048, "neginf", 0.0),
     (4, 4, 2048, "wide", 0.0),
     (2, 2, 2, "cluster", 0.0),
+    # K above 2048: the one-CTA-per-row instantiation for K up to 4096
+    (5, 2, 4096, "zeros", 0.0),
+    (160, 4, 2560, "bf16", 0.0),      # more rows than SMs
+    (4, 4, 4096, "cluster", 0.0),     # pathological buckets: the fallback
+    (3, 4, 4096, "neginf", 0.5),
+    (6, 3, 4096, "ties", 0.05),
+    (2, 4, 3072, "wide", 0.0),
 ]
 
 
