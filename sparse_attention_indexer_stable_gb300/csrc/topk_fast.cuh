@@ -3,33 +3,36 @@
 // 4096 columns and the fused top-K over all shards fall here).
 //
 // A persistent grid walks the rows: CTAs of 512 threads, two per SM, for many
-// rows (one CTA's row streams in from HBM while the other CTA selects), or one
-// 1024-thread CTA per row for a few rows.  A row is staged in shared memory
-// by bulk copies (TMA) read straight from the rank-major layout, and
-// selection and final order come out of one two-level bucket pass instead of
-// a radix select followed by a sort:
+// rows (while one CTA waits at a barrier or on a copy the other computes), or
+// 1024-thread CTAs, one per row or per SM, for few, long or large-K rows.  A
+// row's scores and ids are staged in shared memory by bulk copies (TMA) read
+// straight from the rank-major layout, on separate barriers; the next row's
+// scores are copied as soon as L1 has read this row's.  Selection and final
+// order come out of one two-level bucket pass instead of a radix select
+// followed by a sort:
 //
-//  L1      a 12-bit (11-bit in 1024-thread CTAs) histogram of the score
-//          keys' top bits over every candidate (the "radix pass over 32-bit
-//          score keys first" of
-//          "[Kernel] Optimize CuTeDSL DCP top-k merge", Summary) locates the
-//          bin b1 holding the K-th largest key; bins above b1 are all winners.
-//  COMPACT the candidates of bins >= b1 ("live", about K of them) are packed
-//          into a dense list of 64-bit keys score_key<<32 | ~id.
-//  L2      each live bin is split into fine buckets, about one per two
-//          members, on the next bits of its 64-bit key, skipping bits that
-//          are equal for all live candidates; the token id enters only where
-//          scores tie, which is the page's conditional tie-break.  Buckets are
-//          numbered in key order, so a prefix sum over their sizes gives each
-//          bucket its first output position.
-//  RANK    a live candidate in a bucket that starts before K counts the bucket
-//          members with larger keys (members of shared buckets are first
-//          gathered into the bucket's slice of the live list): its output
-//          position is the bucket start plus that count, and positions >= K
-//          are the losers.  Buckets hold a few members, so this one step both
-//          finishes the selection at the threshold and sorts the winners.
-//          RANK runs over list positions, so a warp's output positions are
-//          consecutive up to a bucket's size and its stores nearly coalesced.
+//  L1       a histogram of the score keys' top 12 bits (11 in 1024-thread
+//           CTAs) over every candidate: the "radix pass over 32-bit score
+//           keys first" of "[Kernel] Optimize CuTeDSL DCP top-k merge",
+//           Summary.
+//  SCAN1    locates the bin b1 holding the K-th largest key (bins above it
+//           are all winners) and gives every bin >= b1 a number of fine
+//           buckets, about one per two keys, and a first bucket.
+//  COMPACT  the candidates of bins >= b1 ("live", about K of them) are packed
+//           into a dense list of 64-bit keys score_key<<32 | ~id.
+//  L2       each live key's fine bucket: its bin's first bucket plus the top
+//           bits of its key below the bin, skipping bits equal for all live
+//           keys; the token id enters only where scores tie, which is the
+//           page's conditional tie-break.  Buckets are numbered in key order.
+//  SCAN2    a prefix sum over bucket sizes gives each bucket its first output
+//           position.
+//  SCATTER  keys of buckets that start before K go to their bucket's slice of
+//           the list.
+//  RANK     per list position: output position = bucket start + the bucket's
+//           members with larger keys; positions >= K are the losers.  Buckets
+//           hold a few keys, so this one step both finishes the selection at
+//           the threshold and sorts the winners.  A warp's positions are
+//           consecutive, so its output stores are nearly coalesced.
 //
 // Rows whose live set or buckets come out too large for this (pathologically
 // clustered keys) take the radix-select + sort of topk_core.cuh on the same
@@ -90,7 +93,7 @@ struct StreamCaps {
 template <int LIVE, int FINE, int BINS>
 struct StreamShared {
   unsigned long long live[LIVE];      // live keys; then in bucket order; fallback: sorted winners
-  uint32_t fine[FINE];                // L2 sizes, then start << 16 | fill cursor
+  uint32_t fine[FINE];                // L2 sizes, then start << 16 | size << 8 | fill cursor
   union {
     uint32_t table[BINS];             // L1 counts, then first bucket << 8 | log2(buckets)
     SelectShared sel;                 // the fallback's radix-select state
@@ -460,11 +463,11 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
 
     const uint32_t b1 = s.b1;
     const int nfine = (int)s.nfine;
-    // Live candidates are those with (key >> kRefShift) >= live_from.  Normally that
-    // is every candidate of bins >= b1; when bin b1 alone is too full for the
-    // live list, its next 11 key bits are histogrammed (in `fine`, still
-    // zero) and only its candidates from the digit holding the K-th key on
-    // are kept live.
+    // Live candidates are those with (key >> kRefShift) >= live_from.
+    // Normally that is every candidate of bins >= b1; when the live set would
+    // overflow the live list, the next 11 key bits of bin b1 are histogrammed
+    // (in `fine`, still zero) and only its candidates from the digit holding
+    // the K-th key on are kept live.
     uint32_t live_from = b1 << 11;
     if (s.nlive > (uint32_t)kLiveMax) {
 #pragma unroll
@@ -715,8 +718,8 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         }
       }
     }
-    // RANK wrote the aux region through ordinary stores; the next row's ids
-    // are copied into it after the barrier.
+    // SCATTER wrote the aux region through ordinary stores; the next row's
+    // ids are copied into it after the barrier.
     if constexpr (Source::kStagesIds) fence_proxy_async_shared();
     __syncthreads();  // every reader of this row's shared state is done
     if constexpr (Source::kStagesIds)
