@@ -26,6 +26,10 @@
  *    when the stream reaches that point; calls issue no host-device sync and
  *    may be captured in a CUDA graph once the device has been used by a
  *    first (uncaptured) call of the same entry point;
+ *  - kernels are launched with programmatic stream serialization: one may be
+ *    scheduled while the stream's previous kernel drains, but it waits for
+ *    that kernel to complete (its writes visible) before touching memory, so
+ *    stream order is unchanged;
  *  - outputs must not overlap inputs;
  *  - argument errors are reported before anything is enqueued.
  */
