@@ -108,6 +108,10 @@ CASES = [
     (4, 4, 2048, "neginf", 0.0),
     (4, 4, 2048, "wide", 0.0),
     (2, 2, 2, "cluster", 0.0),
+    # every candidate in one L1 bin: the live set is refined on the next bits
+    (200, 4, 2048, "narrow", 0.0),    # two CTAs per SM
+    (8, 4, 2048, "narrow", 0.0),      # one CTA per row
+    (3, 4, 4096, "narrow", 0.0),      # K up to 4096
     # K above 2048: the one-CTA-per-row instantiation for K up to 4096
     (5, 2, 4096, "zeros", 0.0),
     (160, 4, 2560, "bf16", 0.0),      # more rows than SMs

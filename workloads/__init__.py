@@ -147,7 +147,7 @@ def random_merge(seed: int, T: int, dcp: int, K: int, mode: str = "normal",
     ``ties`` (4 distinct values), ``const`` (one value), ``zeros`` (+0/-0 and
     a few +-1), ``neginf`` (many real -inf scores), ``wide`` (ids spread over
     the whole non-negative int32 range), ``cluster`` (most top scores within a
-    few ulps of each other).
+    few ulps of each other), ``narrow`` (fp32 scores uniform in [1, 1.0625)).
     pad_frac: fraction of slots, anywhere in each shard, replaced by padding.
     """
     rng = np.random.default_rng(seed)
@@ -187,6 +187,10 @@ def random_merge(seed: int, T: int, dcp: int, K: int, mode: str = "normal",
             if len(pos) > m:
                 flat[t, pos[m]] = np.float32(1.2)
         scores = np.ascontiguousarray(flat.reshape(T, dcp, K).transpose(1, 0, 2))
+    elif mode == "narrow":
+        # fp32 scores uniform in [1, 1 + 1/16): one L1 bin holds every
+        # candidate, with distinct keys below it (the live-set refinement)
+        scores = rng.uniform(1.0, 1.0625, size=shape).astype(np.float32)
     elif mode == "neginf":
         scores = np.where(rng.random(shape) < 0.6, NEG_INF,
                           rng.standard_normal(shape, dtype=np.float32)).astype(np.float32)
