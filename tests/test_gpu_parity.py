@@ -108,6 +108,9 @@ CASES = [
     (4, 4, 2048, "neginf", 0.0),
     (4, 4, 2048, "wide", 0.0),
     (2, 2, 2, "cluster", 0.0),
+    # every candidate a winner (K equals the row's candidates), many rows
+    (200, 1, 2048, "normal", 0.0),
+    (170, 2, 1024, "ties", 0.1),
     # every candidate in one L1 bin: the live set is refined on the next bits
     (200, 4, 2048, "narrow", 0.0),    # two CTAs per SM
     (8, 4, 2048, "narrow", 0.0),      # one CTA per row
