@@ -433,6 +433,8 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
 #pragma unroll
         for (int e = 0; e < kBinsPer; ++e) {
           const uint32_t above = ex & 0xFFFFu, fabove = ex >> 16;
+          // this and the thread's later bins lie below b1: no table entries
+          if (above >= (uint32_t)ksel) break;
           const int b = kL1Bins - 1 - (kBinsPer * tid + e);
           if (h[e] != 0u) {
             if (above < (uint32_t)ksel && (uint32_t)ksel <= above + h[e]) {
