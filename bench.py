@@ -448,12 +448,18 @@ def decode_and_sweep(torch, dk, dev, stream):
         def fused():
             dk.fused_topk(logits, K, out_scores=fo_s, out_ids=fo_i, stream=stream)
 
+        def fused_inter():
+            dk.fused_topk(logits, K, out_scores=fo_s, out_ids=fo_i, stream=stream,
+                          layout="interleaved")
+
         sweep[str(T)] = {"us_per_step_launch": median_of_reps(torch, fn, stream, launches=50),
                          "us_per_step_graph": median_of_reps(torch, fn, stream, launches=50,
                                                              graph=True),
                          "fused_us_per_launch": median_of_reps(torch, fused, stream, launches=50),
                          "fused_us_per_graph_replay": median_of_reps(torch, fused, stream,
-                                                                     launches=50, graph=True)}
+                                                                     launches=50, graph=True),
+                         "fused_interleaved_us_per_graph_replay": median_of_reps(
+                             torch, fused_inter, stream, launches=50, graph=True)}
     out["sweep_local4_plus_merge_and_fused"] = sweep
     return out
 
