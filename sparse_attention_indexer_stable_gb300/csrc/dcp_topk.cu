@@ -96,6 +96,13 @@ struct MergeSource {
     const int r = i / K;
     return ~(uint32_t)__ldg(ids + ((size_t)r * T + t) * (size_t)K + (i - r * K));
   }
+  // Score keys of candidates 4c .. 4c+3 of row t (one shard: K % 4 == 0).
+  __device__ uint4 key4_global(int t, int c) const {
+    const int i = 4 * c, r = i / K;
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(scores + ((size_t)r * T + t) * (size_t)K +
+                                                         (i - r * K)));
+    return make_uint4(score_key(w.x), score_key(w.y), score_key(w.z), score_key(w.w));
+  }
 
   // Per-row part of the output id, read once per row.
   __device__ uint32_t row_base(int t) const {

@@ -37,7 +37,10 @@
 // Rows whose live set or buckets come out too large for this (pathologically
 // clustered keys) take the radix-select + sort of topk_core.cuh on the same
 // row (read again from global memory): the result never depends on the
-// data's distribution, only the speed does.
+// data's distribution, only the speed does.  Merge rows with fewer real
+// candidates than K, the rest padding (-inf, -1) from shards shorter than K,
+// land there too (the padding keys are all alike): they only sort their real
+// candidates and fill the tail with padding.
 //
 // Barriers: shared state is reset only after the barrier that follows its last
 // reader in the row (the race the first page's review reports came from
@@ -55,6 +58,7 @@ constexpr int kStreamMaxN = 8192;             // candidates per row (two CTAs pe
 constexpr int kStreamMaxNWide = 16384;        // candidates per row (one CTA per SM)
 constexpr int kStreamMaxK = 2048;             // K of the regular instantiations
 constexpr int kStreamMaxKWide = 4096;         // K of the one-CTA-per-row instantiation for larger K
+constexpr uint32_t kNegInfKey = 0x007FFFFFu;  // score key of -inf: padding's, with ~id 0
 constexpr uint32_t kBigBucket = 255;          // a larger bucket starting before K sends the row to the fallback
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr unsigned long long kStageWaitLimit = 1ull << 31;  // cycles (about 1 s) to wait for a row's copy
@@ -77,7 +81,7 @@ struct StreamCaps {
   static constexpr int kL1Bins = 1 << kL1Bits;
   static constexpr uint32_t kLowMask = (1u << kL1Shift) - 1u;  // key bits below the L1 bin
   static constexpr int kRefShift = kL1Shift - 11;  // the refinement digit: 11 bits below the bin
-  static constexpr uint32_t kPadBin = 0x007FFFFFu >> kL1Shift;  // bin of -inf keys (padding)
+  static constexpr uint32_t kPadBin = kNegInfKey >> kL1Shift;  // bin of -inf keys (padding)
   static constexpr int kLive = NT == 512 ? 2560 : KMAX + 1024;
   static constexpr int kFine = NT == 512 ? 2560 : KMAX + 1024;
   // fine buckets per L1 bin; the bins above b1 hold fewer than K keys and
@@ -110,6 +114,7 @@ struct StreamShared {
   uint32_t found_digit, found_above, found_count;  // refinement of b1
   uint32_t p_end;                     // end of the bucket straddling K
   uint32_t overflow;                  // a bucket to rank is too large
+  uint32_t pad_n;                     // fallback: padding keys of the row
   unsigned long long stage_bar;       // completes when a row's scores land in the stage
   unsigned long long ids_bar;         // completes when a row's ids land in the aux region
 };
@@ -293,6 +298,92 @@ __device__ __forceinline__ void zero_words(uint32_t* p, int words) {
     *reinterpret_cast<uint4*>(p + i) = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// The fallback for one row of the streaming kernel: the row again from
+// global memory, radix select + sort (topk_core.cuh).  Merge rows whose K-th
+// key is -inf with fewer candidates above the padding key than K, the rest
+// padding (-inf, -1) from shards shorter than K (alike keys, so too large a
+// bucket for the fast path), sort just those candidates and pad the tail.
+// Out of line: rare, and its code stays out of the row loop.  Every thread of
+// the CTA calls it; the staged ids are intact (only SCATTER overwrites them).
+template <int NT, int KMAX, class Source, class Shared>
+__device__ __noinline__ void fallback_row(const Source src, Shared& s, const uint32_t* aux, int t,
+                                          int n, int ksel, int K, float* os, int32_t* oi) {
+  using Caps = StreamCaps<NT, KMAX>;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int n4 = n >> 2;
+  int nwin = ksel;  // winners in s.live[0, nwin), sorted; padding after them
+  bool sorted = false;
+  if constexpr (Source::kStagesIds) {
+    if (s.b1 == Caps::kPadBin) {
+      if (tid == 0) s.live_cursor = 0u;  // COMPACT's last use was barriers ago
+      __syncthreads();
+      uint32_t npad = 0u;
+#pragma unroll 1
+      for (int c0 = 0; c0 < n4; c0 += NT) {
+        const int c = c0 + tid;
+        uint4 k4 = make_uint4(0u, 0u, 0u, 0u), u4 = k4;
+        if (c < n4) {
+          k4 = src.key4_global(t, c);
+          u4 = src.inv4(aux, c);
+        }
+        const uint32_t ks[4] = {k4.x, k4.y, k4.z, k4.w};
+        const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
+        uint32_t m = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (c < n4) {
+            if (ks[e] > kNegInfKey || (ks[e] == kNegInfKey && us[e] != 0u)) m |= 1u << e;
+            npad += (ks[e] == kNegInfKey && us[e] == 0u) ? 1u : 0u;
+          }
+        }
+        const uint32_t cnt = __popc(m);
+        const uint32_t incl = warp_inclusive_scan(cnt);
+        uint32_t base = 0u;
+        if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
+        uint32_t slot = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (m & (1u << e)) {
+            if (slot < (uint32_t)Caps::kLive) s.live[slot] = ((unsigned long long)ks[e] << 32) | us[e];
+            ++slot;
+          }
+        }
+      }
+      npad = __reduce_add_sync(0xFFFFFFFFu, npad);
+      if (lane == 0 && npad != 0u) atomicAdd(&s.pad_n, npad);
+      __syncthreads();
+      const uint32_t nreal = s.live_cursor;  // candidates above the padding key
+      if (nreal < (uint32_t)ksel && nreal + s.pad_n >= (uint32_t)ksel) {
+        int n_pow2 = 1;
+        while (n_pow2 < (int)nreal) n_pow2 <<= 1;
+        for (int j = (int)nreal + tid; j < n_pow2; j += NT) s.live[j] = 0ull;
+        __syncthreads();
+        bitonic_sort_desc<NT>(s.live, n_pow2);
+        nwin = (int)nreal;
+        sorted = true;
+      }
+    }
+  }
+  if (!sorted) {
+    int n_pow2 = 1;
+    while (n_pow2 < ksel) n_pow2 <<= 1;
+    select_sort_row<NT>(
+        s.u.sel, n, ksel, s.live, n_pow2, [&](int i) { return src.key_global(t, i); },
+        [&](int i) { return src.inv_global(t, i); });
+  }
+  const uint32_t rbase = src.row_base(t);
+  for (int j = tid; j < K; j += NT) {
+    if (j < nwin) {
+      const unsigned long long w = s.live[j];
+      os[j] = __uint_as_float(score_bits((uint32_t)(w >> 32)));
+      oi[j] = src.out_id_from(rbase, (uint32_t)w);
+    } else {
+      os[j] = __uint_as_float(0xFF800000u);  // -inf
+      oi[j] = -1;
+    }
+  }
+}
+
 template <int NT, int MAXN, int KMAX, class Source>
 __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     topk_stream_kernel(Source src, int T, int K, float* __restrict__ out_scores,
@@ -334,6 +425,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     s.live_cursor = 0u;
     s.p_end = 0u;
     s.overflow = 0u;
+    s.pad_n = 0u;
     s.stat_or[0] = s.stat_or[1] = 0u;
     s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
   }
@@ -702,23 +794,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         oi[j] = -1;
       }
     } else {
-      // ---- Fallback: radix select + sort, reading the row from global memory -
-      int n_pow2 = 1;
-      while (n_pow2 < ksel) n_pow2 <<= 1;
-      select_sort_row<NT>(
-          s.u.sel, n, ksel, s.live, n_pow2, [&](int i) { return src.key_global(t, i); },
-          [&](int i) { return src.inv_global(t, i); });
-      const uint32_t rbase = src.row_base(t);
-      for (int j = tid; j < K; j += NT) {
-        if (j < ksel) {
-          const unsigned long long w = s.live[j];
-          os[j] = __uint_as_float(score_bits((uint32_t)(w >> 32)));
-          oi[j] = src.out_id_from(rbase, (uint32_t)w);
-        } else {
-          os[j] = __uint_as_float(0xFF800000u);
-          oi[j] = -1;
-        }
-      }
+      fallback_row<NT, KMAX>(src, s, aux, t, n, ksel, K, os, oi);
     }
     // SCATTER wrote the aux region through ordinary stores; the next row's
     // ids are copied into it after the barrier.
@@ -732,6 +808,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       s.live_cursor = 0u;
       s.p_end = 0u;
       s.overflow = 0u;
+      s.pad_n = 0u;
       s.stat_or[0] = s.stat_or[1] = 0u;
       s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
     }

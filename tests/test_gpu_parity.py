@@ -122,6 +122,15 @@ CASES = [
     (3, 4, 4096, "neginf", 0.5),
     (6, 3, 4096, "ties", 0.05),
     (2, 4, 3072, "wide", 0.0),
+    # fewer real candidates than K (short shards): the K-th key is padding
+    (16, 4, 2048, "normal", 0.8),     # one CTA per row
+    (200, 4, 2048, "bf16", 0.8),      # two CTAs per SM
+    (200, 4, 2048, "normal", 0.95),
+    (4, 4, 2048, "neginf", 0.8),      # real -inf candidates above the padding
+    (160, 4, 2048, "neginf", 0.7),
+    (3, 4, 4096, "ties", 0.8),        # K up to 4096
+    (3, 8, 2048, "normal", 0.9),      # 16384 candidates per row
+    (5, 4, 1024, "const", 0.9),
 ]
 
 
@@ -131,6 +140,58 @@ def test_random_shapes(case):
     m = workloads.random_merge(zlib.crc32(repr(case).encode()) & 0xFFFF, T, dcp, K, mode=mode, pad_frac=pad,
                                with_row_starts=(T % 2 == 0))
     assert_same(run_merge(m), oracle.merge(m.scores, m.ids, m.row_starts), str(case))
+
+
+def _nan_padding_merge(T, dcp=4, K=2048, seed=7):
+    """Rows mixing real candidates, padding and NaNs of both signs.
+
+    Per row (cycling): only real finite candidates and padding; plus negative
+    NaNs (which rank below padding) where the padding still fills K; so many
+    negative NaNs that the padding does not (the NaNs are winners); positive
+    NaNs (which rank above +inf); real -inf candidates above the padding.
+    """
+    rng = np.random.default_rng(seed)
+    n = dcp * K
+    ids = workloads.distinct_ids(rng, dcp, T, K, 1 << 20)
+    flat_s = np.empty((T, n), np.float32)
+    flat_i = ids.transpose(1, 0, 2).reshape(T, n).copy()
+    neg_nan = lambda m: (np.uint32(0xFF800001) + rng.integers(0, 0x7FFFFE, m).astype(np.uint32)).view(np.float32)
+    pos_nan = lambda m: (np.uint32(0x7F800001) + rng.integers(0, 0x7FFFFE, m).astype(np.uint32)).view(np.float32)
+    for t in range(T):
+        real = int(rng.integers(1, K // 2))
+        kind = t % 5
+        row = np.full(n, -np.inf, np.float32)
+        pad = np.ones(n, bool)
+        perm = rng.permutation(n)
+        row[perm[:real]] = rng.standard_normal(real).astype(np.float32)
+        pad[perm[:real]] = False
+        rest = perm[real:]
+        if kind == 1:    # a few negative NaNs, padding still fills K
+            m = 50
+        elif kind == 2:  # negative NaNs leave padding just enough
+            m = n - K
+        elif kind == 3:  # padding falls short: negative NaNs are winners
+            m = n - real - (K - real) // 2
+        else:
+            m = 0
+        if m:
+            row[rest[:m]] = neg_nan(m)
+            pad[rest[:m]] = False
+        if kind == 4:    # positive NaNs and real -inf candidates
+            row[rest[:40]] = pos_nan(40)
+            pad[rest[:40]] = False
+            pad[rest[40:40 + K // 2]] = False  # real -inf: keep their ids
+        flat_s[t] = row
+        flat_i[t] = np.where(pad, -1, flat_i[t])
+    scores = np.ascontiguousarray(flat_s.reshape(T, dcp, K).transpose(1, 0, 2))
+    ids = np.ascontiguousarray(flat_i.reshape(T, dcp, K).transpose(1, 0, 2))
+    return workloads.Merge("nan-padding", scores, ids, np.arange(T, dtype=np.int32) * 3)
+
+
+@pytest.mark.parametrize("T", [10, 200])
+def test_nans_and_padding(T):
+    m = _nan_padding_merge(T)
+    assert_same(run_merge(m), oracle.merge(m.scores, m.ids, m.row_starts), f"T={T}")
 
 
 def test_all_padding_rows():

@@ -90,6 +90,21 @@ def test_merge_brute_force(seed):
     assert np.array_equal(_bits(out_scores[0]), _bits(np.array([s for s, _ in want], np.float32)))
 
 
+def test_merge_nan_order():
+    """NaNs take the place their bits give them in the score key order (a
+    reading: the pages never meet a NaN): sign clear above +inf, sign set
+    below -inf and below padding.  Worked by hand for one row, K = 6."""
+    bits = np.array([0xFFC00000, 0x3F800000, 0xFF800000, 0x7FC00001, 0xFF800000, 0x7F800000],
+                    np.uint32)
+    scores = bits.view(np.float32).reshape(1, 1, 6)
+    ids = np.array([4, 9, -1, 2, 5, 7], np.int32).reshape(1, 1, 6)
+    out_ids, out_scores = oracle.merge(scores, ids)
+    # +NaN (2), +inf (7), 1.0 (9), real -inf (5), padding, -NaN (4)
+    assert out_ids[0].tolist() == [2, 7, 9, 5, -1, 4]
+    assert _bits(out_scores[0]).tolist() == [0x7FC00001, 0x7F800000, 0x3F800000, 0xFF800000,
+                                             0xFF800000, 0xFFC00000]
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_merge_permutation_invariance(seed):
     rng = np.random.default_rng(2000 + seed)
