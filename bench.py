@@ -252,11 +252,26 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample": sample},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_cpu()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def host_cpu() -> dict:
+    """The host the CPU oracle runs on: architecture, logical cores, model."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"machine": platform.machine(), "nproc": os.cpu_count(), "model": model}
 
 
 def run_ours(args):
@@ -339,7 +354,7 @@ def run_ours(args):
         v, rows, secs = cpu_oracle_sample(m, budget_s=args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{rows} rows of the prefill workload ({secs:.1f} s), single-threaded "
-                         f"C oracle"}
+                         f"C oracle", "host": host_cpu()}
 
     if rank == 0:
         line = {

@@ -13,7 +13,9 @@ mathematics rather than by the oracle itself:
   equals the top-K over all shards' logits at once, with contiguous and with
   interleaved shard ids;
 * the two shard id layouts give different, hand-worked orders
-  (tests/golden/fused_examples.txt).
+  (tests/golden/fused_examples.txt);
+* a library cross-check: numpy's sort of the same 64-bit keys selects and
+  orders the same K winners at full row sizes.
 
 A plausible mistake in the oracle (a missing inversion of negative keys, a
 signed instead of unsigned id order, row_starts on padding, a dropped shard,
@@ -103,6 +105,28 @@ def test_merge_nan_order():
     assert out_ids[0].tolist() == [2, 7, 9, 5, -1, 4]
     assert _bits(out_scores[0]).tolist() == [0x7FC00001, 0x7F800000, 0x3F800000, 0xFF800000,
                                              0xFF800000, 0xFFC00000]
+
+
+@pytest.mark.parametrize("mode,pad", [("ties", 0.1), ("normal", 0.8), ("zeros", 0.0), ("neginf", 0.3)])
+def test_merge_matches_library_sort(mode, pad):
+    """The oracle's selection and order against numpy's sort of the same
+    64-bit keys (the keys themselves are pinned by the hand-worked examples
+    and the float-comparison brute force above): a mistake in the oracle's
+    gather, comparator, cut at K or id mapping fails here at full size."""
+    m = workloads.random_merge(77, 5, 4, 512, mode=mode, pad_frac=pad, with_row_starts=True)
+    out_ids, out_scores = oracle.merge(m.scores, m.ids, m.row_starts)
+    bits = _bits(m.scores).astype(np.uint64)
+    key32 = np.where(bits >> np.uint64(31), ~bits & np.uint64(0xFFFFFFFF), bits | np.uint64(0x80000000))
+    inv = (~m.ids.astype(np.int64)) & 0xFFFFFFFF
+    key64 = (key32 << np.uint64(32)) | inv.astype(np.uint64)
+    for t in range(m.T):
+        k = key64[:, t, :].reshape(-1)
+        order = np.argsort(k, kind="stable")[::-1][: m.K]
+        ids = m.ids[:, t, :].reshape(-1)[order].astype(np.int64)
+        want_ids = np.where(ids == -1, -1, ids + int(m.row_starts[t]))
+        want_scores = m.scores[:, t, :].reshape(-1)[order]
+        assert out_ids[t].tolist() == want_ids.tolist()
+        assert np.array_equal(_bits(out_scores[t]), _bits(want_scores))
 
 
 @pytest.mark.parametrize("seed", range(6))
