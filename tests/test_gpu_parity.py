@@ -301,6 +301,10 @@ LOCAL_CASES = [
     (3, 100, 100, 200, "normal"),   # L < K: padded
     (2, 7, 7, 7, "ties"),
     (33, 4096, 4096, 2048, "ties"),
+    (160, 4096, 4096, 2048, "normal"),  # more rows than SMs
+    (8, 4096, 4096, 2048, "masked"),    # causal mask: real -inf candidates
+    (160, 4096, 4096, 2048, "masked"),
+    (4, 16384, 16384, 4096, "masked"),
 ]
 
 
@@ -364,6 +368,8 @@ FUSED_CASES = [
     (2, 2, 60, 60, 200, "bf16"),       # fewer candidates than K: padded
     (160, 4, 4096, 4096, 2048, "bf16"),  # more rows than SMs
     (3, 8, 2048, 2048, 2048, "ties"),
+    (6, 4, 4096, 4096, 2048, "masked"),  # real -inf candidates
+    (160, 2, 4096, 4096, 2048, "masked"),
 ]
 
 

@@ -207,7 +207,13 @@ def random_merge(seed: int, T: int, dcp: int, K: int, mode: str = "normal",
 
 
 def random_logits(seed: int, T: int, L: int, ld: int | None = None, mode: str = "bf16") -> np.ndarray:
-    """Logits rows (T, ld) with the first L columns meaningful."""
+    """Logits rows (T, ld) with the first L columns meaningful.
+
+    mode: ``bf16`` (N(0,1) rounded to bf16), ``normal`` (fp32 N(0,1)),
+    ``ties`` (4 distinct values), ``masked`` (bf16 values in each row's first
+    columns, a row-dependent count from 0 to L, and -inf after them: a causal
+    mask).
+    """
     rng = np.random.default_rng(seed)
     ld = L if ld is None else ld
     x = rng.standard_normal((T, ld), dtype=np.float32)
@@ -215,6 +221,10 @@ def random_logits(seed: int, T: int, L: int, ld: int | None = None, mode: str = 
         x = round_to_bf16(x)
     elif mode == "ties":
         x = np.array([0.75, 0.5, -0.25, 2.0], np.float32)[rng.integers(0, 4, (T, ld))]
+    elif mode == "masked":
+        x = round_to_bf16(x)
+        valid = rng.integers(0, L + 1, T)
+        x[np.arange(ld)[None, :] >= valid[:, None]] = NEG_INF
     elif mode != "normal":
         raise ValueError(mode)
     return np.ascontiguousarray(x, dtype=np.float32)
