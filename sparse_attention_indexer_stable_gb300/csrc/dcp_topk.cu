@@ -60,6 +60,8 @@ struct MergeSource {
   // copies straight from the rank-major layout (needs K % 4 == 0 and
   // 16-byte aligned bases), completing on separate barriers.
   static constexpr bool kStagesIds = true;
+  // ids are arbitrary: their order is not the candidates' order
+  __device__ bool index_ordered() const { return false; }
   __host__ __device__ int score_words() const { return dcp * K; }
   __host__ __device__ int ids_words() const { return dcp * K; }
 
@@ -156,6 +158,7 @@ struct LocalSource {
 
   // Ids are column numbers: only the logits are staged.
   static constexpr bool kStagesIds = false;
+  __device__ bool index_ordered() const { return true; }  // ids grow with the column
   __host__ __device__ int score_words() const { return L; }
   __host__ __device__ int ids_words() const { return 0; }
 
@@ -225,6 +228,8 @@ struct FusedSource {
 
   // Ids are r*L + c: only the logits are staged.
   static constexpr bool kStagesIds = false;
+  // ids grow with the candidate index only in the contiguous layout
+  __device__ bool index_ordered() const { return !interleaved; }
   __host__ __device__ int score_words() const { return dcp * L; }
   __host__ __device__ int ids_words() const { return 0; }
 

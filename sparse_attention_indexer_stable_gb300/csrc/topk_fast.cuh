@@ -299,10 +299,16 @@ __device__ __forceinline__ void zero_words(uint32_t* p, int words) {
 }
 
 // The fallback for one row of the streaming kernel: the row again from
-// global memory, radix select + sort (topk_core.cuh).  Merge rows whose K-th
-// key is -inf with fewer candidates above the padding key than K, the rest
-// padding (-inf, -1) from shards shorter than K (alike keys, so too large a
-// bucket for the fast path), sort just those candidates and pad the tail.
+// global memory, radix select + sort (topk_core.cuh).  Two kinds of rows
+// whose K-th key is -inf take a shorter way:
+// - merge rows with fewer candidates above the padding key than K, the rest
+//   padding (-inf, -1) from shards shorter than K (alike keys, so too large a
+//   bucket for the fast path): just those candidates are sorted and the tail
+//   padded;
+// - rows of logits with fewer finite values than K (a masked row), where ids
+//   grow with the candidate index: the finite candidates are sorted, and the
+//   -inf winners, the lowest ids among the -inf candidates, are the first
+//   ones in index order, so a running count places them.
 // Out of line: rare, and its code stays out of the row loop.  Every thread of
 // the CTA calls it; the staged ids are intact (only SCATTER overwrites them).
 template <int NT, int KMAX, class Source, class Shared>
@@ -311,7 +317,8 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
   using Caps = StreamCaps<NT, KMAX>;
   const int tid = threadIdx.x, lane = tid & 31;
   const int n4 = n >> 2;
-  int nwin = ksel;  // winners in s.live[0, nwin), sorted; padding after them
+  int nwin = ksel;  // winners in s.live[0, nwin), sorted
+  int tail = ksel;  // padding from here on (positions nwin .. tail are written)
   bool sorted = false;
   if constexpr (Source::kStagesIds) {
     if (s.b1 == Caps::kPadBin) {
@@ -359,7 +366,100 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
         for (int j = (int)nreal + tid; j < n_pow2; j += NT) s.live[j] = 0ull;
         __syncthreads();
         bitonic_sort_desc<NT>(s.live, n_pow2);
-        nwin = (int)nreal;
+        nwin = tail = (int)nreal;
+        sorted = true;
+      }
+    }
+  } else {
+    if (s.b1 == Caps::kPadBin && src.index_ordered()) {
+      if (tid == 0) {
+        s.live_cursor = 0u;
+        s.pad_n = 0u;  // here: the -inf candidates
+      }
+      __syncthreads();
+      uint32_t ninf = 0u;
+#pragma unroll 1
+      for (int c0 = 0; c0 < n4; c0 += NT) {
+        const int c = c0 + tid;
+        uint32_t ks[4] = {0u, 0u, 0u, 0u};
+        if (c < n4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ks[e] = src.key_global(t, 4 * c + e);
+        }
+        const uint4 u4 = src.inv4(aux, c);
+        const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
+        uint32_t m = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (c < n4) {
+            if (ks[e] > kNegInfKey) m |= 1u << e;
+            ninf += ks[e] == kNegInfKey ? 1u : 0u;
+          }
+        }
+        const uint32_t cnt = __popc(m);
+        const uint32_t incl = warp_inclusive_scan(cnt);
+        uint32_t base = 0u;
+        if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
+        uint32_t slot = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (m & (1u << e)) {
+            if (slot < (uint32_t)Caps::kLive) s.live[slot] = ((unsigned long long)ks[e] << 32) | us[e];
+            ++slot;
+          }
+        }
+      }
+      ninf = __reduce_add_sync(0xFFFFFFFFu, ninf);
+      if (lane == 0 && ninf != 0u) atomicAdd(&s.pad_n, ninf);
+      __syncthreads();
+      const uint32_t nf = s.live_cursor;  // candidates above -inf
+      if (nf < (uint32_t)ksel && nf + s.pad_n >= (uint32_t)ksel) {
+        // the first ksel - nf -inf candidates in index order take positions
+        // nf .. ksel
+        constexpr int kWarpsT = NT / 32;
+        const int warp = tid >> 5;
+        const uint32_t need = (uint32_t)ksel - nf;
+        const uint32_t rbase = src.row_base(t);
+        uint32_t before = 0u;  // -inf candidates in earlier chunks
+#pragma unroll 1
+        for (int c0 = 0; c0 < n4 && before < need; c0 += NT) {
+          const int c = c0 + tid;
+          uint32_t f = 0u;
+          if (c < n4) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f |= (src.key_global(t, 4 * c + e) == kNegInfKey ? 1u : 0u) << e;
+          }
+          const uint32_t cnt = __popc(f);
+          const uint32_t incl = warp_inclusive_scan(cnt);
+          if (lane == 31) s.wa[warp] = incl;
+          __syncthreads();
+          const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
+          const uint32_t wti = warp_inclusive_scan(wt);
+          const uint32_t chunk = __shfl_sync(0xFFFFFFFFu, wti, kWarpsT - 1);
+          uint32_t q = before + __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - cnt;
+          if (f != 0u) {
+            const uint4 u4 = src.inv4(aux, c);
+            const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (f & (1u << e)) {
+                if (q < need) {
+                  os[nf + q] = __uint_as_float(0xFF800000u);  // -inf
+                  oi[nf + q] = src.out_id_from(rbase, us[e]);
+                }
+                ++q;
+              }
+            }
+          }
+          before += chunk;
+          __syncthreads();  // s.wa is rewritten by the next chunk
+        }
+        int n_pow2 = 1;
+        while (n_pow2 < (int)nf) n_pow2 <<= 1;
+        for (int j = (int)nf + tid; j < n_pow2; j += NT) s.live[j] = 0ull;
+        __syncthreads();
+        bitonic_sort_desc<NT>(s.live, n_pow2);
+        nwin = (int)nf;
         sorted = true;
       }
     }
@@ -377,7 +477,7 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
       const unsigned long long w = s.live[j];
       os[j] = __uint_as_float(score_bits((uint32_t)(w >> 32)));
       oi[j] = src.out_id_from(rbase, (uint32_t)w);
-    } else {
+    } else if (j >= tail) {
       os[j] = __uint_as_float(0xFF800000u);  // -inf
       oi[j] = -1;
     }
