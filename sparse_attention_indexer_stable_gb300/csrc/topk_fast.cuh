@@ -37,10 +37,10 @@
 // Rows whose live set or buckets come out too large for this (pathologically
 // clustered keys) take the radix-select + sort of topk_core.cuh on the same
 // row (read again from global memory): the result never depends on the
-// data's distribution, only the speed does.  Merge rows with fewer real
-// candidates than K, the rest padding (-inf, -1) from shards shorter than K,
-// land there too (the padding keys are all alike): they only sort their real
-// candidates and fill the tail with padding.
+// data's distribution, only the speed does.  Rows whose K-th key is -inf
+// land there too and take a shorter way (fallback_row): merge rows with fewer
+// real candidates than K, the rest padding (-inf, -1) from shards shorter than
+// K, and masked rows of logits with fewer finite values than K.
 //
 // Barriers: shared state is reset only after the barrier that follows its last
 // reader in the row (the race the first page's review reports came from
