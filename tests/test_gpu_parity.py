@@ -49,6 +49,38 @@ def test_named_workloads(name):
     assert_same(run_merge(m), oracle.merge(m.scores, m.ids, m.row_starts), name)
 
 
+# The hand-worked examples of tests/golden/, run through the CUDA path and
+# compared with their worked-out values (not only with the oracle).
+@pytest.mark.parametrize("ex", helpers.parse_merge_examples(), ids=lambda e: e["name"])
+def test_merge_golden_on_gpu(ex):
+    out_ids, out_scores = dk.merge(_dev(ex["scores_in"]), _dev(ex["ids_in"]),
+                                   None if ex["rs"] is None else _dev(ex["rs"]))
+    torch.cuda.synchronize()
+    assert out_ids.cpu().numpy()[0].tolist() == ex["ids"]
+    assert np.array_equal(_bits(out_scores.cpu().numpy()[0]), _bits(np.array(ex["scores"], np.float32)))
+
+
+@pytest.mark.parametrize("ex", helpers.parse_local_examples(), ids=lambda e: e["name"])
+def test_local_golden_on_gpu(ex):
+    rs = None if ex["row_starts"] is None else _dev(np.array([ex["row_starts"]], np.int32))
+    out_scores, out_ids = dk.local_topk(_dev(ex["row"]), ex["K"], ex["rank"], ex["dcp"], L=ex["L"],
+                                        row_starts=rs,
+                                        layout="interleaved" if ex.get("interleaved") else "contiguous")
+    torch.cuda.synchronize()
+    assert out_ids.cpu().numpy()[0].tolist() == ex["ids"]
+    assert np.array_equal(_bits(out_scores.cpu().numpy()[0]), _bits(np.array(ex["scores"], np.float32)))
+
+
+@pytest.mark.parametrize("ex", helpers.parse_fused_examples(), ids=lambda e: e["name"])
+def test_fused_golden_on_gpu(ex):
+    rs = None if ex["row_starts"] is None else _dev(np.array([ex["row_starts"]], np.int32))
+    out_scores, out_ids = dk.fused_topk(_dev(ex["logits"]), ex["K"], L=ex["L"], row_starts=rs,
+                                        layout="interleaved" if ex.get("interleaved") else "contiguous")
+    torch.cuda.synchronize()
+    assert out_ids.cpu().numpy()[0].tolist() == ex["ids"]
+    assert np.array_equal(_bits(out_scores.cpu().numpy()[0]), _bits(np.array(ex["scores"], np.float32)))
+
+
 @pytest.mark.parametrize("seed", range(24))
 def test_tieheavy_many_seeds(seed):
     """Heavy ties at the threshold across many seeds: the regression check for
