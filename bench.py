@@ -219,6 +219,36 @@ def cpu_oracle_sample(m, budget_s=10.0):
             return rows_done / el, rows_done, el
 
 
+def cpu_oracle_sample_threads(m, threads, budget_s=5.0):
+    """The same oracle, unchanged, on `threads` host threads at once, each on
+    its own rows (rows are independent; the C call releases the GIL): the
+    whole host's throughput.  Returns (rows/s, rows, seconds)."""
+    import concurrent.futures
+
+    import oracle
+
+    oracle.build()
+    order = np.random.default_rng(2).permutation(m.T)
+    batch = 16
+    counts = [0] * threads
+    stop = time.perf_counter() + budget_s
+
+    def work(k):
+        i = k * batch
+        while time.perf_counter() < stop:
+            start = i % m.T
+            rows = order[start:start + batch]
+            oracle.merge(m.scores, m.ids, m.row_starts, rows=rows)
+            counts[k] += len(rows)
+            i += threads * batch
+
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(threads) as pool:
+        list(pool.map(work, range(threads)))
+    el = time.perf_counter() - t0
+    return sum(counts) / el, sum(counts), el
+
+
 def run_reference(args):
     rank = env_int("RANK", 0)
     if rank != 0:
@@ -349,12 +379,17 @@ def run_ours(args):
     e2e = None
     if not args.skip_extras and not args.workload.startswith("sweep"):
         e2e = end_to_end(torch, dk, m, dev, stream, steps=max(3, min(20, args.steps)))
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and world == 1 and not args.skip_extras and not args.workload.startswith("sweep"):
         v, rows, secs = cpu_oracle_sample(m, budget_s=args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{rows} rows of the prefill workload ({secs:.1f} s), single-threaded "
                          f"C oracle", "host": host_cpu()}
+        threads = os.cpu_count() or 1
+        vt, rows_t, secs_t = cpu_oracle_sample_threads(m, threads)
+        cpu_all = {"value": vt, "unit": UNIT, "cores": threads, "kind": "oracle",
+                   "sample": f"{rows_t} rows of the prefill workload ({secs_t:.1f} s), the same "
+                             f"C oracle on {threads} threads, rows split between them"}
 
     if rank == 0:
         line = {
@@ -373,6 +408,7 @@ def run_ours(args):
                          "traffic": profiled_traffic() if args.workload == "prefill" else None,
                          "algorithmic_bytes": alg_bytes},
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
             "e2e": e2e,
             "gpu_launches": args.steps,
             "clocks": clk.summary(),

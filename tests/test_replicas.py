@@ -88,3 +88,15 @@ def test_reference_arm_json_line():
     assert d["unit"] == "rows/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_oracle_throughput_on_all_host_cores():
+    """The whole-host oracle figure runs the same oracle on several threads,
+    each on its own rows, and counts every row it merged."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+
+    m = workloads.random_merge(3, 64, 4, 256, mode="bf16")
+    v, rows, secs = bench.cpu_oracle_sample_threads(m, 2, budget_s=0.5)
+    assert rows > 0 and secs > 0 and abs(v - rows / secs) < 1e-6 * v
