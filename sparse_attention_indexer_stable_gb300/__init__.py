@@ -147,15 +147,22 @@ def _torch():
 
 
 def _stream_handle(stream, dev=None):
+    """The cudaStream_t to launch on: `stream` (a torch stream or a raw
+    handle), else the current stream of device index `dev`."""
     if stream is None:
-        stream = _torch().cuda.current_stream(dev)
+        torch = _torch()
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:  # the handle itself, without a Stream object
+            return raw(torch.cuda.current_device() if dev is None else dev)
+        stream = torch.cuda.current_stream(dev)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _ok(t, dtype, device):
-    """Fast form of _check: True when t needs no complaint."""
+    """Fast form of _check: True when t needs no complaint (device: an index
+    or None)."""
     return (t.dtype == dtype and t.is_cuda and t.is_contiguous()
-            and (device is None or t.device == device))
+            and (device is None or t.get_device() == device))
 
 
 def _check(t, name, dtype, device):
@@ -166,16 +173,18 @@ def _check(t, name, dtype, device):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_cuda or (device is not None and t.device != device):
-        raise ValueError(f"{name} must be on {device or 'a CUDA device'}")
+    if not t.is_cuda or (device is not None and t.get_device() != device):
+        where = "a CUDA device" if device is None else f"cuda:{device}"
+        raise ValueError(f"{name} must be on {where}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
 
 
 def _on_device(dev, fn):
-    """Run fn with dev current (the library works on the current device)."""
+    """Run fn with device index dev current (the library works on the
+    current device)."""
     torch = _torch()
-    if dev.index == torch.cuda.current_device():
+    if dev == torch.cuda.current_device():
         return fn()
     with torch.cuda.device(dev):
         return fn()
@@ -190,7 +199,7 @@ def merge(scores, ids, row_starts=None, out_ids=None, out_scores=None, stream=No
     """
     torch = _torch()
     _check(scores, "scores", torch.float32, None)
-    dev = scores.device
+    dev = scores.get_device()
     _check(ids, "ids", torch.int32, dev)
     if scores.dim() != 3 or ids.shape != scores.shape:
         raise ValueError("scores and ids must both be (dcp, T, K)")
@@ -239,7 +248,7 @@ def local_topk(logits, K, rank, dcp, L=None, row_starts=None, out_scores=None, o
         raise TypeError("logits must be a float32 CUDA tensor")
     if logits.dim() != 2 or logits.stride(1) != 1:
         raise ValueError("logits must be 2-D with unit column stride")
-    dev = logits.device
+    dev = logits.get_device()
     T = logits.shape[0]
     ld = logits.stride(0) if T > 1 else logits.shape[1]
     L = logits.shape[1] if L is None else int(L)
@@ -280,7 +289,7 @@ def fused_topk(logits, K, L=None, row_starts=None, out_scores=None, out_ids=None
         raise TypeError("logits must be a float32 CUDA tensor")
     if logits.dim() != 3 or not logits.is_contiguous():
         raise ValueError("logits must be a contiguous (dcp, T, ld) tensor")
-    dev = logits.device
+    dev = logits.get_device()
     dcp, T, ld = logits.shape
     L = ld if L is None else int(L)
     if L > ld:
