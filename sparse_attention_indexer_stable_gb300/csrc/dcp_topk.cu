@@ -7,10 +7,12 @@
 #include <cstdint>
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include "dcp_topk.h"
 #include "topk_core.cuh"
 #include "topk_fast.cuh"
+#include "topk_rows.cuh"
 
 namespace dcp {
 
@@ -104,6 +106,22 @@ struct MergeSource {
     const uint4 w = __ldg(reinterpret_cast<const uint4*>(scores + ((size_t)r * T + t) * (size_t)K +
                                                          (i - r * K)));
     return make_uint4(score_key(w.x), score_key(w.y), score_key(w.z), score_key(w.w));
+  }
+
+  // Ids of candidates 4c .. 4c+3 of row t (one shard: K % 4 == 0).
+  __device__ uint4 ids4_global(int t, int c) const {
+    const int i = 4 * c, r = i / K;
+    return __ldg(reinterpret_cast<const uint4*>(ids + ((size_t)r * T + t) * (size_t)K + (i - r * K)));
+  }
+
+  // One thread: pulls row t's scores and ids of every shard into L2.
+  __device__ void prefetch_row(int t) const {
+    const size_t stride = (size_t)T * (size_t)K;
+    const size_t off = (size_t)t * (size_t)K;
+    for (int r = 0; r < dcp; ++r) {
+      prefetch_l2(scores + off + r * stride, (uint32_t)K * 4u);
+      prefetch_l2(ids + off + r * stride, (uint32_t)K * 4u);
+    }
   }
 
   // Per-row part of the output id, read once per row.
@@ -397,6 +415,9 @@ static cudaError_t device_info(DeviceInfo** out) {
     if ((e = allow_stream_kernels<MergeSource>(smem)) != cudaSuccess) return e;
     if ((e = allow_stream_kernels<LocalSource>(smem)) != cudaSuccess) return e;
     if ((e = allow_stream_kernels<FusedSource>(smem)) != cudaSuccess) return e;
+    if ((e = allow_max_smem(merge_rows_kernel<MergeSource>, (int)sizeof(RowsShared))) !=
+        cudaSuccess)
+      return e;
     if ((e = status_word(&d.status)) != cudaSuccess) return e;
     d.configured.store(true, std::memory_order_release);
   }
@@ -441,7 +462,9 @@ __global__ void wait_timeout_selftest_kernel(unsigned long long limit, unsigned 
   if (__syncthreads_or(!ok) && threadIdx.x == 0) atomicOr(status, kStatusCopyTimeout);
 }
 
-// Streaming path when the row fits it (n <= 8192, K <= 2048, 16-byte copies
+// The many-row merge at K = 2048 (more rows than SMs, dcp <= 4, 16-byte
+// aligned rows): four 256-thread CTAs per SM walking the rows.  Otherwise the
+// streaming path when the row fits it (n <= 16384, K <= 4096, 16-byte copies
 // possible): one 1024-thread CTA per row when the rows fit on the SMs at
 // once, else two 512-thread CTAs per SM walking the rows.  The general path
 // otherwise.
@@ -464,6 +487,15 @@ static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out
                          smem <= (size_t)d->max_smem_optin;
   const int grid1 = T < d->sms ? T : d->sms;
   cudaError_t e;
+  if constexpr (std::is_same<Source, MergeSource>::value) {
+    if (src.vec4 && K == kRowsK && n <= kRowsMaxN && T > d->sms &&
+        sizeof(RowsShared) <= (size_t)d->max_smem_optin) {
+      const int grid = T < 4 * d->sms ? T : 4 * d->sms;
+      e = launch_serialized(merge_rows_kernel<MergeSource>, grid, kRowsNT, sizeof(RowsShared),
+                            stream, src, T, out_scores, out_ids);
+      return e == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+    }
+  }
   if (stream_ok && big_k) {
     e = launch_serialized(topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxKWide, Source>,
                           grid1, 1024, smem, stream, src, T, K, out_scores, out_ids, d->status);

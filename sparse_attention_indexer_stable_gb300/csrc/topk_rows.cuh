@@ -1,0 +1,631 @@
+// topk_rows.cuh -- the many-row merge at K = 2048 (prefill-scale merges: more
+// rows than SMs, dcp <= 4 shards of 2048 candidates each).
+//
+// Four 256-thread CTAs share an SM, each walking the rows
+// t = blockIdx.x + k*gridDim.x (the 1024-row chunks of "Reserve the sparse
+// indexer's DCP top-k merge scratch through the workspace manager", Purpose,
+// visited in order; rows are independent).  Four rows in flight per SM keep
+// the SM busy while any one CTA sits in a short serial step of its row.  No
+// row is staged in shared memory: each thread reads its 32 candidates with
+// 16-byte coalesced loads straight from the rank-major (dcp, T, K) buffers,
+// and the next row is prefetched into L2 about a third of a row ahead (early
+// enough to land, late enough to stay: a whole row ahead it was evicted again
+// and DRAM read 45% more than the candidates).
+//
+// Per row ("[Kernel] Optimize CuTeDSL DCP top-k merge", Summary: a radix pass
+// over 32-bit score keys first, the id tie-break only where scores tie):
+//  L1       histogram of the score keys' top 12 bits (4096 bins).
+//  SCAN1    every warp sums four 128-bin windows; every warp then scans the
+//           32 window totals and ranks the bins of its windows at or above
+//           the window holding the K-th key: bin b gets above(b), the number
+//           of candidates in higher bins, and count(b).  The bin b1 with
+//           above(b1) < K <= above(b1) + count(b1) holds the K-th key.
+//  COMPACT  candidates of bins >= b1 ("live", about K + a part of b1) are
+//           packed as 64-bit keys score_key << 32 | ~id; the ids are read
+//           here.  A bin b1 too full for the list is refined first on its
+//           next 11 key bits.
+//  L2       buckets in position space: bin b owns buckets
+//           [above(b), above(b) + count(b)), one per candidate, and each live
+//           key goes to the bucket named by the top bits of its key below the
+//           bin, the varying low bits of ~id joining only below equal score
+//           bits (the conditional tie-break).  Buckets are numbered in key
+//           order.
+//  SCAN2    prefix sum of bucket sizes: each bucket's first output position.
+//  SCATTER  keys of buckets starting before K take a slot in their bucket's
+//           range, with a rank key that orders the bucket's members.
+//  RANK     per list position: output position = bucket start + the members
+//           ranking above; positions >= K are the losers.  A warp's positions
+//           are consecutive, so its output stores are nearly coalesced.
+//
+// Rows whose buckets come out too large (more than 255 keys in one, e.g.
+// keys clustered within a few ulps) or whose K-th key is in the -inf bin take
+// the radix select + sort of topk_core.cuh on the same row (rows_fallback):
+// the result never depends on the data's distribution, only the speed does.
+//
+// Barriers: shared state is reset only after the barrier that follows its
+// last reader in the row (the race the first page's review reports came from
+// resetting shared state that late warps had not yet read).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "topk_core.cuh"
+#include "topk_fast.cuh"
+
+namespace dcp {
+
+constexpr int kRowsNT = 256;             // threads per CTA (four CTAs per SM)
+constexpr int kRowsK = 2048;             // K of this kernel
+constexpr int kRowsMaxN = 8192;          // candidates per row: dcp <= 4
+constexpr int kRowsL1Shift = 20;         // L1 bins: the score key's top 12 bits
+constexpr int kRowsBins = 4096;
+constexpr int kRowsLive = 2560;          // live list (a fuller bin b1 is refined first)
+constexpr int kRowsFine = kRowsLive;     // position-space buckets: one per live key
+constexpr int kRowsRankMax = kRowsK + 256;  // list positions: up to the end of the bucket straddling K
+constexpr int kRowsRankWords = (kRowsRankMax + 8) * 2;  // 64-bit rank keys, + a window's overrun
+constexpr int kRowsRegionWords = kRowsRankWords + kRowsRankMax / 2;  // + u16 bucket info
+constexpr uint32_t kRowsPadBin = kNegInfKey >> kRowsL1Shift;  // bin of -inf keys (padding)
+
+struct RowsShared {
+  uint32_t fine[kRowsFine];            // L2 bucket sizes, then start << 16 | size << 8 | fill cursor
+  uint32_t region[kRowsRegionWords];   // L1 histogram, then the bin table; after L2 RANK's scratch;
+                                       // the fallback's radix-select state
+  unsigned long long live[kRowsLive];  // live keys; the fallback's sorted winners
+  uint32_t wa[kMaxWarps];
+  uint32_t wb[kMaxWarps];              // SCAN1: window totals
+  uint32_t stat_or[2];                 // OR of the raw scores' bits below the bin; OR of live ~ids
+  uint32_t stat_and[2];                // [1]: AND of live ~ids (padding's 0 left out)
+  uint32_t live_cursor;
+  uint32_t b1;                         // L1 bin of the K-th largest key
+  uint32_t nlive;                      // candidates in bins >= b1 (after refinement: live)
+  uint32_t above_b1;                   // candidates in bins above b1
+  uint32_t found_digit, found_above, found_count;  // refinement of b1
+  uint32_t p_end;                      // end of the bucket straddling K
+  uint32_t overflow;                   // a bucket to rank is too large
+  uint32_t pad_cnt;                    // candidates in the -inf bin
+  uint32_t pad_n;                      // fallback: padding candidates
+};
+static_assert(offsetof(RowsShared, region) == sizeof(uint32_t) * kRowsFine,
+              "fine and the histogram are one region to reset");
+static_assert(offsetof(RowsShared, region) % 16 == 0 && offsetof(RowsShared, live) % 16 == 0,
+              "16-byte vector accesses");
+static_assert(kRowsRegionWords >= kRowsBins, "histogram");
+static_assert(sizeof(SelectShared) <= sizeof(uint32_t) * kRowsRegionWords, "fallback state");
+static_assert(kRowsLive >= kRowsK && kRowsRankMax >= kRowsK + (int)kBigBucket - 1, "caps");
+
+// Starts pulling `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint4 ldg4(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// The fallback for one row: the row again from global memory, radix select +
+// sort (topk_core.cuh).  A row whose K-th key is padding and that has fewer
+// candidates above the padding key than K (shards shorter than K, padded
+// with (-inf, -1): one bucket of identical keys, too large for the fast
+// path) takes a shorter way: just those candidates are sorted and the tail
+// padded.  Out of line: rare, and its code stays out of the row loop.  Every
+// thread of the CTA calls it.
+template <class Source>
+__device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int t, int n,
+                                           float* os, int32_t* oi) {
+  constexpr int NT = kRowsNT;
+  constexpr int ksel = kRowsK;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int n4 = n >> 2;
+  int nwin = ksel, tail = ksel;  // winners in s.live[0, nwin), sorted; padding from tail on
+  bool sorted = false;
+  SelectShared& sel = *reinterpret_cast<SelectShared*>(s.region);
+  if (s.b1 == kRowsPadBin) {
+    if (tid == 0) {
+      s.live_cursor = 0u;
+      s.pad_n = 0u;
+    }
+    __syncthreads();
+    uint32_t npad = 0u;
+#pragma unroll 1
+    for (int c0 = 0; c0 < n4; c0 += NT) {
+      const int c = c0 + tid;
+      uint4 k4 = make_uint4(0u, 0u, 0u, 0u), u4 = k4;
+      if (c < n4) {
+        k4 = src.key4_global(t, c);
+        const uint4 i4 = src.ids4_global(t, c);
+        u4 = make_uint4(~i4.x, ~i4.y, ~i4.z, ~i4.w);
+      }
+      const uint32_t ks[4] = {k4.x, k4.y, k4.z, k4.w};
+      const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
+      uint32_t m = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (c < n4) {
+          if (ks[e] > kNegInfKey || (ks[e] == kNegInfKey && us[e] != 0u)) m |= 1u << e;
+          npad += (ks[e] == kNegInfKey && us[e] == 0u) ? 1u : 0u;
+        }
+      }
+      const uint32_t cnt = __popc(m);
+      const uint32_t incl = warp_inclusive_scan(cnt);
+      uint32_t base = 0u;
+      if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
+      uint32_t slot = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (m & (1u << e)) {
+          if (slot < (uint32_t)kRowsLive) s.live[slot] = ((unsigned long long)ks[e] << 32) | us[e];
+          ++slot;
+        }
+      }
+    }
+    npad = __reduce_add_sync(0xFFFFFFFFu, npad);
+    if (lane == 0 && npad != 0u) atomicAdd(&s.pad_n, npad);
+    __syncthreads();
+    const uint32_t nreal = s.live_cursor;  // candidates above the padding key
+    if (nreal < (uint32_t)ksel && nreal + s.pad_n >= (uint32_t)ksel) {
+      int n_pow2 = 1;
+      while (n_pow2 < (int)nreal) n_pow2 <<= 1;
+      for (int j = (int)nreal + tid; j < n_pow2; j += NT) s.live[j] = 0ull;
+      __syncthreads();
+      bitonic_sort_desc<NT>(s.live, n_pow2);
+      nwin = tail = (int)nreal;
+      sorted = true;
+    }
+  }
+  if (!sorted) {
+    select_sort_row<NT>(
+        sel, n, ksel, s.live, ksel, [&](int i) { return src.key_global(t, i); },
+        [&](int i) { return src.inv_global(t, i); });
+  }
+  const uint32_t rbase = src.row_base(t);
+  for (int j = tid; j < ksel; j += NT) {
+    if (j < nwin) {
+      const unsigned long long w = s.live[j];
+      os[j] = __uint_as_float(score_bits((uint32_t)(w >> 32)));
+      oi[j] = src.out_id_from(rbase, (uint32_t)w);
+    } else if (j >= tail) {
+      os[j] = __uint_as_float(0xFF800000u);  // -inf
+      oi[j] = -1;
+    }
+  }
+}
+
+// One CTA of kRowsNT threads per row at a time; grid <= 4 * SMs.  Thread tid
+// owns 16-byte chunk v of the row for v < 2*dcp: shard v/2, chunk
+// tid + 256*(v%2) of the shard's 2048 candidates.
+template <class Source>
+__global__ void __launch_bounds__(kRowsNT, 4)
+    merge_rows_kernel(Source src, int T, float* __restrict__ out_scores,
+                      int32_t* __restrict__ out_ids) {
+  constexpr int NT = kRowsNT;
+  constexpr int kWarpsT = NT / 32;          // 8
+  constexpr int kVec = kRowsMaxN / 4 / NT;  // 16-byte chunks per thread: 8
+  constexpr int kItems = 4 * kVec;          // candidates per thread: 32
+  constexpr int kLivePer = kRowsLive / NT;  // 10
+  constexpr int kFinePer = kRowsFine / NT;  // 10
+  constexpr int kWindows = kRowsBins / 128;  // 32 windows of 128 bins
+  constexpr int K = kRowsK;
+  constexpr int ksel = kRowsK;
+  constexpr int kL1Shift = kRowsL1Shift;
+  constexpr uint32_t kLowMask = (1u << kL1Shift) - 1u;  // key bits below the bin
+  constexpr int kRefShift = kL1Shift - 11;  // the refinement digit: 11 bits below the bin
+
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  RowsShared& s = *reinterpret_cast<RowsShared*>(smem_raw);
+  uint32_t* table = s.region;
+  // RANK's scratch in the region (free after L2): wide rows 64-bit rank keys,
+  // narrow rows 32-bit rank keys and list indices; bucket info for both.
+  unsigned long long* rk64 = reinterpret_cast<unsigned long long*>(s.region);
+  uint32_t* rk32 = s.region;
+  uint16_t* pidx = reinterpret_cast<uint16_t*>(s.region + kRowsRankMax + 8);
+  uint16_t* info = reinterpret_cast<uint16_t*>(s.region + kRowsRankWords);
+  const int n = src.count();  // dcp * 2048
+  const int n4 = n >> 2;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const size_t shard_stride = (size_t)T * (size_t)K;  // elements between shards
+
+  // Shared-memory set-up first: it touches no global memory, so it may run
+  // while the stream's previous kernel is still finishing.
+  zero_words<NT>(s.fine, kRowsFine + kRowsBins);  // fine and the histogram behind it
+  if (tid == 0) {
+    s.live_cursor = 0u;
+    s.p_end = 0u;
+    s.overflow = 0u;
+    s.stat_or[0] = s.stat_or[1] = 0u;
+    s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
+  }
+  const int G = (int)gridDim.x;
+  int t = (int)blockIdx.x;
+  grid_dependency_wait();  // every thread, before its first global access
+  if (tid == 0 && t < T) src.prefetch_row(t);
+
+  for (; t < T; t += G) {
+    const float* srow = src.scores + (size_t)t * K;
+    const int32_t* irow = src.ids + (size_t)t * K;
+    uint4 w[kVec];
+#pragma unroll
+    for (int v = 0; v < kVec; ++v)
+      w[v] = (tid + v * NT) < n4
+                 ? ldg4(srow + (size_t)(v >> 1) * shard_stride + 4 * (tid + NT * (v & 1)))
+                 : make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();  // the previous row's shared state is reset
+
+    // ---- L1: histogram of the score keys' top 12 bits ----------------------
+    // Also ORs the raw scores' bits below the bin: the bits that are zero in
+    // all of them are constant in every key of one sign (bf16-valued scores
+    // leave the low 16 zero), which the buckets below skip.
+    uint32_t keys[kItems];
+    uint32_t raw_or = 0u;
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+      if ((tid + v * NT) < n4) {  // uniform across the CTA: v < 2*dcp
+        raw_or |= w[v].x | w[v].y | w[v].z | w[v].w;
+        keys[4 * v + 0] = score_key(w[v].x);
+        keys[4 * v + 1] = score_key(w[v].y);
+        keys[4 * v + 2] = score_key(w[v].z);
+        keys[4 * v + 3] = score_key(w[v].w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) atomicAdd(&table[keys[4 * v + e] >> kL1Shift], 1u);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) keys[4 * v + e] = 0u;
+      }
+    }
+    raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & kLowMask);
+    if (lane == 0 && raw_or) atomicOr(&s.stat_or[0], raw_or);
+    __syncthreads();
+
+    // ---- SCAN1a: candidates per window of 128 bins (warp w: windows 4w..4w+3)
+#pragma unroll
+    for (int j = 0; j < kWindows / kWarpsT; ++j) {
+      const int win = warp * (kWindows / kWarpsT) + j;
+      const uint4 h4 = *reinterpret_cast<const uint4*>(table + 128 * win + 4 * lane);
+      const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, h4.x + h4.y + h4.z + h4.w);
+      if (lane == 0) s.wb[win] = sum;
+    }
+    if (tid == 0) s.pad_cnt = table[kRowsPadBin];
+    __syncthreads();
+    // ---- SCAN1b: every warp scans the window totals, high to low, then ranks
+    // the bins of its own windows at or above the window holding the K-th
+    // key: table[b] = above(b) | count(b) << 11 | log2ceil(count(b)) << 25.
+    {
+      const uint32_t wt = s.wb[kWindows - 1 - lane];  // lane l: window 31 - l
+      const uint32_t wincl = warp_inclusive_scan(wt);
+#pragma unroll
+      for (int j = 0; j < kWindows / kWarpsT; ++j) {
+        const int win = warp * (kWindows / kWarpsT) + j;
+        const uint32_t above_w = __shfl_sync(0xFFFFFFFFu, wincl - wt, kWindows - 1 - win);
+        const uint32_t tot_w = __shfl_sync(0xFFFFFFFFu, wt, kWindows - 1 - win);
+        if (tot_w == 0u || above_w >= (uint32_t)ksel) continue;
+        const int hi = 128 * win + 127;  // lane l: bins hi-4l .. hi-4l-3
+        uint32_t h[4];
+        load_bins_desc<4>(table + (hi - 4 * lane - 3), h);
+        const uint32_t local = h[0] + h[1] + h[2] + h[3];
+        const uint32_t incl = warp_inclusive_scan(local);
+        uint32_t a = above_w + incl - local;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (h[e] != 0u && a < (uint32_t)ksel) {
+            const int b = hi - 4 * lane - e;
+            if ((uint32_t)ksel <= a + h[e]) {
+              s.b1 = (uint32_t)b;
+              s.nlive = a + h[e];
+              s.above_b1 = a;
+            }
+            const uint32_t q = h[e] > 1u ? 32u - __clz(h[e] - 1u) : 0u;
+            table[b] = a | (h[e] << 11) | (q << 25);
+          }
+          a += h[e];
+        }
+      }
+    }
+    __syncthreads();
+
+    // Live candidates are those with (key >> kRefShift) >= live_from: every
+    // candidate of bins >= b1, unless that overflows the live list; then the
+    // next 11 key bits of bin b1 are histogrammed (in `fine`, still zero) and
+    // only its candidates from the digit holding the K-th key on stay live.
+    const uint32_t b1 = s.b1;
+    uint32_t live_from = b1 << 11;
+    if (s.nlive > (uint32_t)kRowsLive) {
+#pragma unroll
+      for (int j = 0; j < kItems; ++j) {
+        if ((tid + (j >> 2) * NT) < n4 && (keys[j] >> kL1Shift) == b1)
+          atomicAdd(&s.fine[(keys[j] >> kRefShift) & 0x7FFu], 1u);
+      }
+      __syncthreads();
+      find_digit_desc<NT>(s.fine, (uint32_t)ksel - s.above_b1, s.wa, s.wb, s.found_digit,
+                          s.found_above, s.found_count);
+      __syncthreads();
+      live_from |= s.found_digit;
+      const uint32_t hb = s.found_above + s.found_count;  // live candidates of bin b1
+      zero_words<NT>(s.fine, kHistBins);
+      __syncthreads();
+      if (tid == 0) {
+        s.nlive = s.above_b1 + hb;
+        const uint32_t q = hb > 1u ? 32u - __clz(hb - 1u) : 0u;
+        table[b1] = s.above_b1 | (hb << 11) | (q << 25);
+      }
+      __syncthreads();
+    }
+    const int nlive = (int)s.nlive;
+    bool fast = nlive <= kRowsLive;
+    const bool has_pad = s.pad_cnt != 0u;
+
+    // ---- COMPACT: live candidates into a dense list ------------------------
+    if (fast) {
+      uint32_t mask = 0u;
+      const uint32_t lf = live_from << kRefShift;  // live: key >= lf
+      if (lf != 0u) {
+        // candidates past the row hold key 0 (< lf)
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) mask |= (keys[j] >= lf ? 1u : 0u) << j;
+      } else {
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) mask |= ((tid + (j >> 2) * NT) < n4 ? 1u : 0u) << j;
+      }
+      const uint32_t cnt = __popc(mask);
+      const uint32_t incl = warp_inclusive_scan(cnt);
+      uint32_t base = 0u;
+      if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
+      unsigned long long* dst = s.live + (__shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt);
+      // OR / AND of the row's inverted ids (padding's ~id of 0 left out: it
+      // is the smallest, so ordering on the varying bits alone still puts
+      // it last)
+      uint32_t ior = 0u, iand = 0xFFFFFFFFu;
+#pragma unroll
+      for (int v = 0; v < kVec; ++v) {
+        if ((tid + v * NT) < n4) {
+          const uint4 iv = ldg4(irow + (size_t)(v >> 1) * shard_stride + 4 * (tid + NT * (v & 1)));
+          const uint32_t us[4] = {~iv.x, ~iv.y, ~iv.z, ~iv.w};
+          ior |= us[0] | us[1] | us[2] | us[3];
+          if (has_pad)
+            iand &= (us[0] ? us[0] : 0xFFFFFFFFu) & (us[1] ? us[1] : 0xFFFFFFFFu) &
+                    (us[2] ? us[2] : 0xFFFFFFFFu) & (us[3] ? us[3] : 0xFFFFFFFFu);
+          else
+            iand &= us[0] & us[1] & us[2] & us[3];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (mask & (1u << (4 * v + e)))
+              *dst++ = ((unsigned long long)keys[4 * v + e] << 32) | us[e];
+        }
+      }
+      ior = __reduce_or_sync(0xFFFFFFFFu, ior);
+      iand = __reduce_and_sync(0xFFFFFFFFu, iand);
+      if (lane == 0) {
+        atomicOr(&s.stat_or[1], ior);
+        atomicAnd(&s.stat_and[1], iand);
+      }
+    }
+    __syncthreads();
+
+    // ---- L2: the position-space bucket of every live candidate -------------
+    // For finite scores the key bits below the L1 bin and below tzf are equal
+    // within a sign, and the bits of ~id at or above ibf are equal for every
+    // candidate of the row (but padding), so within one bin keys are ordered
+    // like y = (low key bits >> tzf) << ibf | (~id low ibf bits), a wf-bit
+    // number; its top q = log2ceil(count) bits, scaled onto the bin's count
+    // buckets, name the bucket.  Bins up to kRowsPadBin (-inf, where padding
+    // lives, and below) keep every bit.  Narrow rows (every live key above
+    // that bin, wf <= 24) rank with 32-bit keys.
+    const uint32_t ro = s.stat_or[0];
+    const uint32_t vi = s.stat_or[1] ^ s.stat_and[1];
+    const int tzf = ro ? min(__ffs(ro) - 1, kL1Shift) : kL1Shift;
+    const int ibf = vi ? 32 - __clz(vi) : 0;
+    const uint32_t imask = ibf >= 32 ? 0xFFFFFFFFu : ((1u << ibf) - 1u);
+    const int wf = kL1Shift - tzf + ibf;
+    const bool narrow = b1 > kRowsPadBin && wf <= 24;
+    uint32_t gsl[kLivePer];
+    if (fast && narrow) {
+#pragma unroll
+      for (int u = 0; u < kLivePer; ++u) {
+        const int e = tid + u * NT;
+        gsl[u] = kNone;
+        if (e < nlive) {
+          const unsigned long long lk = s.live[e];
+          const uint32_t kk = (uint32_t)(lk >> 32);
+          const uint32_t tb = table[kk >> kL1Shift];
+          const int q = (int)(tb >> 25);
+          const uint32_t y = (((kk & kLowMask) >> tzf) << ibf) | ((uint32_t)lk & imask);
+          const int d = wf - q;
+          const uint32_t sub = d >= 0 ? (y >> d) : (y << (-d));
+          const uint32_t cb = (tb >> 11) & 0x3FFFu;
+          const uint32_t g = (tb & 0x7FFu) + cb - 1u - ((sub * cb) >> q);
+          atomicAdd(&s.fine[g], 1u);
+          gsl[u] = g;
+        }
+      }
+    } else if (fast) {
+#pragma unroll
+      for (int u = 0; u < kLivePer; ++u) {
+        const int e = tid + u * NT;
+        gsl[u] = kNone;
+        if (e < nlive) {
+          const unsigned long long lk = s.live[e];
+          const uint32_t kk = (uint32_t)(lk >> 32);
+          const uint32_t inv = (uint32_t)lk;
+          const uint32_t bin = kk >> kL1Shift;
+          const uint32_t tb = table[bin];
+          const int q = (int)(tb >> 25);
+          unsigned long long y;
+          int wy;
+          if (bin > kRowsPadBin) {
+            y = ((unsigned long long)((kk & kLowMask) >> tzf) << ibf) | (inv & imask);
+            wy = wf;
+          } else {
+            y = ((unsigned long long)(kk & kLowMask) << 32) | inv;
+            wy = kL1Shift + 32;
+          }
+          const uint32_t sub = wy >= q ? (uint32_t)(y >> (wy - q)) : (uint32_t)(y << (q - wy));
+          const uint32_t cb = (tb >> 11) & 0x3FFFu;
+          const uint32_t g = (tb & 0x7FFu) + cb - 1u - ((sub * cb) >> q);
+          atomicAdd(&s.fine[g], 1u);
+          gsl[u] = g;
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- SCAN2: bucket starts over positions [0, nlive) ---------------------
+    // fine[g] becomes start << 16 | min(size, 255) << 8, its low byte the
+    // fill cursor for SCATTER.
+    if (fast) {
+      // warps whose buckets all lie past the last one only report a zero total
+      const bool warp_busy = kFinePer * 32 * warp < nlive;
+      uint32_t c[kFinePer];
+      uint32_t local = 0u, incl = 0u;
+      uint32_t* my = s.fine + kFinePer * tid;
+      if (warp_busy) {
+#pragma unroll
+        for (int e = 0; e < kFinePer; e += 2) {
+          const uint2 v2 = *reinterpret_cast<const uint2*>(my + e);
+          c[e] = v2.x;
+          c[e + 1] = v2.y;
+        }
+#pragma unroll
+        for (int e = 0; e < kFinePer; ++e) local += c[e];
+        incl = warp_inclusive_scan(local);
+      }
+      if (lane == 31) s.wa[warp] = incl;
+      __syncthreads();
+      if (warp_busy) {
+        const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
+        const uint32_t wti = warp_inclusive_scan(wt);
+        uint32_t st = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
+        uint32_t over = 0u;
+        uint32_t wv[kFinePer];
+#pragma unroll
+        for (int e = 0; e < kFinePer; ++e) {
+          wv[e] = (st << 16) | (min(c[e], 255u) << 8);
+          if (st < (uint32_t)ksel) {
+            if (c[e] > kBigBucket) over = 1u;
+            if ((uint32_t)ksel <= st + c[e]) s.p_end = st + c[e];
+          }
+          st += c[e];
+        }
+#pragma unroll
+        for (int e = 0; e < kFinePer; e += 2)
+          *reinterpret_cast<uint2*>(my + e) = make_uint2(wv[e], wv[e + 1]);
+        over = __reduce_or_sync(0xFFFFFFFFu, over);
+        if (lane == 0 && over) s.overflow = 1u;
+      }
+    }
+    __syncthreads();
+    fast = fast && s.overflow == 0u;
+
+    // the next row into L2 now: it lands during SCATTER and RANK and stays
+    // there until the next row's loads
+    if (tid == 0 && t + G < T) src.prefetch_row(t + G);
+    float* os = out_scores + (size_t)t * (size_t)K;
+    int32_t* oi = out_ids + (size_t)t * (size_t)K;
+    const uint32_t rbase = fast ? src.row_base(t) : 0u;
+    if (fast && narrow) {
+      // ---- SCATTER: rank key y << 8 | (255 - slot); members of a bucket
+      // share y's top bits, so y orders them, identical keys by their slot.
+#pragma unroll
+      for (int u = 0; u < kLivePer; ++u) {
+        if (gsl[u] != kNone) {
+          const uint32_t old = atomicAdd(&s.fine[gsl[u]], 1u);
+          if ((old >> 16) < (uint32_t)ksel) {
+            const uint32_t pos = (old >> 16) + (old & 0xFFu);
+            const uint32_t e = (uint32_t)(tid + u * NT);
+            info[pos] = (uint16_t)(old & 0xFFFFu);
+            pidx[pos] = (uint16_t)e;
+            const unsigned long long lk = s.live[e];
+            const uint32_t kk = (uint32_t)(lk >> 32);
+            const uint32_t y = (((kk & kLowMask) >> tzf) << ibf) | ((uint32_t)lk & imask);
+            rk32[pos] = (y << 8) | (255u - (old & 0xFFu));
+          }
+        }
+      }
+      __syncthreads();
+      // ---- RANK: position = bucket start + members ranking above ---------
+      const uint32_t p_end = min(s.p_end, (uint32_t)kRowsRankMax);
+      for (uint32_t p = tid; p < p_end; p += NT) {
+        const uint32_t inf = info[p];
+        const uint32_t cnt = inf >> 8;
+        const uint32_t st = p - (inf & 0xFFu);
+        const uint32_t mine = rk32[p];
+        const uint32_t mc = __reduce_max_sync(__activemask(), cnt);
+        uint32_t r = 0u;
+        if (mc > 1u) {
+          const uint32_t* b = rk32 + st;
+          if (mc <= 4u) {
+#pragma unroll
+            for (uint32_t e = 0; e < 4u; ++e) r += (e < cnt && b[e] > mine) ? 1u : 0u;
+          } else if (mc <= 8u) {
+#pragma unroll
+            for (uint32_t e = 0; e < 8u; ++e) r += (e < cnt && b[e] > mine) ? 1u : 0u;
+          } else {
+            for (uint32_t e = 0; e < cnt; ++e) r += b[e] > mine ? 1u : 0u;
+          }
+        }
+        const uint32_t fin = st + r;
+        if (fin < (uint32_t)ksel) {
+          const unsigned long long key = s.live[pidx[p]];
+          os[fin] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
+          oi[fin] = src.out_id_from(rbase, (uint32_t)key);
+        }
+      }
+    } else if (fast) {
+      // ---- SCATTER: rank key (key without its L1 bin) << 12 | list index;
+      // members of a bucket share their key's top 12 bits.
+#pragma unroll
+      for (int u = 0; u < kLivePer; ++u) {
+        if (gsl[u] != kNone) {
+          const uint32_t old = atomicAdd(&s.fine[gsl[u]], 1u);
+          if ((old >> 16) < (uint32_t)ksel) {
+            const uint32_t pos = (old >> 16) + (old & 0xFFu);
+            const uint32_t e = (uint32_t)(tid + u * NT);
+            info[pos] = (uint16_t)(old & 0xFFFFu);
+            rk64[pos] = (s.live[e] << 12) | e;
+          }
+        }
+      }
+      __syncthreads();
+      // ---- RANK ----------------------------------------------------------
+      const uint32_t p_end = min(s.p_end, (uint32_t)kRowsRankMax);
+      for (uint32_t p = tid; p < p_end; p += NT) {
+        const uint32_t inf = info[p];
+        const uint32_t cnt = inf >> 8;
+        const uint32_t st = p - (inf & 0xFFu);
+        const unsigned long long mine = rk64[p];
+        const uint32_t mc = __reduce_max_sync(__activemask(), cnt);
+        uint32_t r = 0u;
+        if (mc > 1u) {
+          const unsigned long long* b = rk64 + st;
+          if (mc <= 4u) {
+#pragma unroll
+            for (uint32_t e = 0; e < 4u; ++e) r += (e < cnt && b[e] > mine) ? 1u : 0u;
+          } else if (mc <= 8u) {
+#pragma unroll
+            for (uint32_t e = 0; e < 8u; ++e) r += (e < cnt && b[e] > mine) ? 1u : 0u;
+          } else {
+            for (uint32_t e = 0; e < cnt; ++e) r += b[e] > mine ? 1u : 0u;
+          }
+        }
+        const uint32_t fin = st + r;
+        if (fin < (uint32_t)ksel) {
+          const unsigned long long key = s.live[(uint32_t)mine & 0xFFFu];
+          os[fin] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
+          oi[fin] = src.out_id_from(rbase, (uint32_t)key);
+        }
+      }
+    } else {
+      rows_fallback(src, s, t, n, os, oi);
+    }
+    __syncthreads();  // every reader of this row's shared state is done
+    zero_words<NT>(s.fine, kRowsFine + kRowsBins);  // fine and the histogram behind it
+    if (tid == 0) {
+      s.live_cursor = 0u;
+      s.p_end = 0u;
+      s.overflow = 0u;
+      s.stat_or[0] = s.stat_or[1] = 0u;
+      s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
+    }
+  }
+}
+
+}  // namespace dcp
