@@ -474,18 +474,15 @@ __global__ void __launch_bounds__(kRowsNT, 4)
     if (fast) {
       // warps whose buckets all lie past the last one only report a zero total
       const bool warp_busy = kFinePer * 32 * warp < nlive;
-      uint32_t c[kFinePer];
+      static_assert(kFinePer % 2 == 0, "8-byte bucket pairs");
       uint32_t local = 0u, incl = 0u;
       uint32_t* my = s.fine + kFinePer * tid;
       if (warp_busy) {
 #pragma unroll
         for (int e = 0; e < kFinePer; e += 2) {
           const uint2 v2 = *reinterpret_cast<const uint2*>(my + e);
-          c[e] = v2.x;
-          c[e + 1] = v2.y;
+          local += v2.x + v2.y;
         }
-#pragma unroll
-        for (int e = 0; e < kFinePer; ++e) local += c[e];
         incl = warp_inclusive_scan(local);
       }
       if (lane == 31) s.wa[warp] = incl;
@@ -495,19 +492,25 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         const uint32_t wti = warp_inclusive_scan(wt);
         uint32_t st = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
         uint32_t over = 0u;
-        uint32_t wv[kFinePer];
-#pragma unroll
-        for (int e = 0; e < kFinePer; ++e) {
-          wv[e] = (st << 16) | (min(c[e], 255u) << 8);
+        // The sizes are read again rather than kept from the first pass: the
+        // row's bucket ids (gsl) are live across this scan, and registers
+        // are what limit four CTAs per SM.
+        auto start = [&](uint32_t c) {
+          const uint32_t w = (st << 16) | (min(c, 255u) << 8);
           if (st < (uint32_t)ksel) {
-            if (c[e] > kBigBucket) over = 1u;
-            if ((uint32_t)ksel <= st + c[e]) s.p_end = st + c[e];
+            if (c > kBigBucket) over = 1u;
+            if ((uint32_t)ksel <= st + c) s.p_end = st + c;
           }
-          st += c[e];
-        }
+          st += c;
+          return w;
+        };
 #pragma unroll
-        for (int e = 0; e < kFinePer; e += 2)
-          *reinterpret_cast<uint2*>(my + e) = make_uint2(wv[e], wv[e + 1]);
+        for (int e = 0; e < kFinePer; e += 2) {
+          const uint2 v2 = *reinterpret_cast<const uint2*>(my + e);
+          const uint32_t w0 = start(v2.x);
+          const uint32_t w1 = start(v2.y);
+          *reinterpret_cast<uint2*>(my + e) = make_uint2(w0, w1);
+        }
         over = __reduce_or_sync(0xFFFFFFFFu, over);
         if (lane == 0 && over) s.overflow = 1u;
       }

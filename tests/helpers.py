@@ -6,6 +6,7 @@ oracle's and to the CUDA path's outputs.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import itertools
 import math
 import os
@@ -207,3 +208,23 @@ def check_merge_invariants(scores, ids, row_starts, out_ids, out_scores, rows=No
 
 def merge_inputs_from_example(ex):
     return ex["scores_in"], ex["ids_in"], ex["rs"]
+
+
+def oracle_merge_all(m, threads=None):
+    """The oracle's merge of every row of merge problem ``m``, the rows split
+    between host threads (rows are independent; the C call releases Python's
+    lock).  Same result as one ``oracle.merge`` call over all rows."""
+    import oracle
+
+    threads = threads or os.cpu_count() or 1
+    T = m.T
+    chunk = max(1, -(-T // (4 * threads)))
+    starts = list(range(0, T, chunk))
+
+    def part(a):
+        rows = np.arange(a, min(T, a + chunk), dtype=np.int32)
+        return oracle.merge(m.scores, m.ids, m.row_starts, rows=rows)
+
+    with concurrent.futures.ThreadPoolExecutor(threads) as pool:
+        parts = list(pool.map(part, starts))
+    return (np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts]))
