@@ -114,6 +114,13 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def wait_first(self, timeout=3.0):
+        """Block until the sampler has produced a line (nvidia-smi takes a
+        moment to start), so that a short timed region is covered."""
+        end = time.perf_counter() + timeout
+        while self.proc is not None and not self.lines and time.perf_counter() < end:
+            time.sleep(0.01)
+
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
@@ -354,11 +361,17 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        clk.wait_first()
         t0 = time.perf_counter()
         evs = time_launches(torch, step, args.steps, stream)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
         barrier()
+        torch.cuda.synchronize(dev)
+        # the same step as 7 repetitions of 200 back-to-back launches (the
+        # first page's protocol; about 0.3 s at prefill size), so the clock
+        # record also covers a long stretch of the kernel
+        us_7x200 = median_of_reps(torch, step, stream, reps=7, launches=200)
         torch.cuda.synchronize(dev)
     per = durations(evs)
     total_ms = evs[0].elapsed_time(evs[-1])
@@ -402,6 +415,7 @@ def run_ours(args):
                        "chunk_rows": 1024, "l2": "inputs 640 MiB > 129 MB L2, no flush",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "us_per_launch": 1000.0 * avg_launch_ms,
+            "us_per_launch_median_7x200": us_7x200,
             "achieved_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,

@@ -93,6 +93,43 @@ dcp_status dcp_topk_merge(const float* scores, const int32_t* ids, int T, int dc
                           void* workspace, size_t workspace_bytes, dcp_stream_t stream);
 
 /*
+ * dcp_topk_merge_shards -- dcp_topk_merge over shards that live in separate
+ * allocations, read where they lie.
+ *
+ * "[DCP][Performance] Add Shared-DCP peer-addressable decode data paths"
+ * (Summary; Top-K performance) has the Top-K consumer read owner-local and
+ * peer shards through views instead of first gathering them into one inbox.
+ * On one GPU that is a merge whose shards are separate buffers: the same
+ * selection and order as dcp_topk_merge, without the copy that would stack
+ * them into a rank-major (dcp, T, K) buffer.
+ *
+ *   shard_scores  DEVICE array of dcp pointers; shard_scores[r] points to
+ *                 fp32 [T][K] row-major: shard r's candidates for row t
+ *                 start at shard_scores[r] + t*K.
+ *   shard_ids     DEVICE array of dcp pointers to int32 [T][K] the same way;
+ *                 -1 marks a padding slot.
+ *   T, dcp, K, row_starts, out_ids, out_scores   as dcp_topk_merge.
+ *
+ * The two pointer arrays are read on the device during the launch, so they
+ * (and the shards) must stay valid and unchanged until the stream passes the
+ * call; a captured CUDA graph reads them again at each replay, so a caller
+ * may repoint shards between replays by rewriting the arrays.  When K is a
+ * multiple of 4 every shard pointer must be 16-byte aligned: the kernels
+ * check this on the device and, if it fails, set
+ * DCP_DEVICE_BAD_SHARD_ALIGNMENT in the device status word
+ * (dcp_topk_device_status) and fill the affected rows with id
+ * DCP_ID_UNWRITTEN and NaN scores instead of reading them.
+ *
+ * Errors: DCP_ERR_INVALID for T < 0, dcp < 1, K < 1, a NULL array or output
+ * with T > 0, or a pointer array the device cannot read (host-only memory);
+ * DCP_ERR_UNSUPPORTED for K > DCP_MAX_K or dcp*K > DCP_MAX_CANDIDATES;
+ * DCP_ERR_CUDA if the launch fails.  No workspace: nothing is staged.
+ */
+dcp_status dcp_topk_merge_shards(const float* const* shard_scores, const int32_t* const* shard_ids,
+                                 int T, int dcp, int K, const int32_t* row_starts,
+                                 int32_t* out_ids, float* out_scores, dcp_stream_t stream);
+
+/*
  * dcp_topk_merge_workspace_size -- scratch bytes dcp_topk_merge needs for
  * these sizes (the merge reserved its scratch through a workspace manager in
  * "Reserve the sparse indexer's DCP top-k merge scratch through the workspace
@@ -192,8 +229,14 @@ dcp_status dcp_fused_topk_ex(const float* logits, int T, int dcp, int L, int ld,
  * dcp_topk_device_status -- reads and clears the device-side status word of
  * the current device.  Kernels that stage rows with bulk copies wait for each
  * copy with a bounded poll (about a second); if a copy never lands, the
- * kernel sets DCP_DEVICE_COPY_TIMEOUT here and its CTA stops, leaving its
- * remaining rows unwritten.  0 means no failure since the last read.
+ * kernel sets DCP_DEVICE_COPY_TIMEOUT here and that CTA stops.  The call that
+ * launched it has already returned DCP_OK, so the status word is the only
+ * report.  The rows that CTA had not finished (its current row and the rows
+ * it would still have walked) are filled with id DCP_ID_UNWRITTEN and a NaN
+ * score; the rest of the call's output is valid.  Before stopping, the CTA
+ * gives its copies one more bounded wait; a copy that still has not landed
+ * may complete into that CTA's (released) shared memory afterwards, so no
+ * wait anywhere is unbounded.  0 means no failure since the last read.
  *
  *   status  host pointer receiving the word (DCP_ERR_INVALID if NULL).
  *
@@ -202,6 +245,8 @@ dcp_status dcp_fused_topk_ex(const float* logits, int T, int dcp, int L, int ld,
  * counterpart on the pages; it is how a bounded wait reports that it gave up.
  */
 #define DCP_DEVICE_COPY_TIMEOUT 1u
+#define DCP_DEVICE_BAD_SHARD_ALIGNMENT 2u /* a separate shard not 16-byte aligned */
+#define DCP_ID_UNWRITTEN INT32_MIN /* id of an output slot a kernel could not fill */
 dcp_status dcp_topk_device_status(unsigned int* status);
 
 /*

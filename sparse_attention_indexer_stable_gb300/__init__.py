@@ -22,8 +22,9 @@ __all__ = [
     "DCP_OK", "DCP_ERR_INVALID", "DCP_ERR_UNSUPPORTED", "DCP_ERR_CUDA",
     "DCP_MAX_K", "DCP_MAX_CANDIDATES", "DcpError",
     "dcp_topk_merge", "dcp_topk_merge_workspace_size", "dcp_local_topk", "dcp_status_string",
+    "dcp_topk_merge_shards", "merge_shards", "DCP_DEVICE_BAD_SHARD_ALIGNMENT",
     "dcp_fused_topk", "dcp_topk_device_status", "dcp_topk_selftest_wait_timeout",
-    "DCP_DEVICE_COPY_TIMEOUT", "fused_topk", "dcp_local_topk_ex", "dcp_fused_topk_ex",
+    "DCP_DEVICE_COPY_TIMEOUT", "DCP_ID_UNWRITTEN", "fused_topk", "dcp_local_topk_ex", "dcp_fused_topk_ex",
     "DCP_IDS_CONTIGUOUS", "DCP_IDS_INTERLEAVED",
     "merge", "local_topk", "library", "library_path",
 ]
@@ -32,6 +33,8 @@ DCP_OK, DCP_ERR_INVALID, DCP_ERR_UNSUPPORTED, DCP_ERR_CUDA = 0, 1, 2, 3
 DCP_MAX_K = 4096
 DCP_MAX_CANDIDATES = 16384
 DCP_DEVICE_COPY_TIMEOUT = 1
+DCP_DEVICE_BAD_SHARD_ALIGNMENT = 2
+DCP_ID_UNWRITTEN = -(1 << 31)  # id of an output slot left by a CTA whose copy timed out
 DCP_IDS_CONTIGUOUS, DCP_IDS_INTERLEAVED = 0, 1
 
 _lock = threading.Lock()
@@ -64,6 +67,8 @@ def library():
             P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             lib.dcp_topk_merge.argtypes = [P, P, I, I, I, P, P, P, P, S, P]
             lib.dcp_topk_merge.restype = I
+            lib.dcp_topk_merge_shards.argtypes = [P, P, I, I, I, P, P, P, P]
+            lib.dcp_topk_merge_shards.restype = I
             lib.dcp_topk_merge_workspace_size.argtypes = [I, I, I, ctypes.POINTER(S)]
             lib.dcp_topk_merge_workspace_size.restype = I
             lib.dcp_local_topk.argtypes = [P, I, I, I, I, I, I, P, P, P, P]
@@ -93,6 +98,12 @@ def dcp_topk_merge(scores, ids, T, dcp, K, row_starts, out_ids, out_scores,
                    workspace=None, workspace_bytes=0, stream=None) -> int:
     return library().dcp_topk_merge(scores, ids, T, dcp, K, row_starts, out_ids, out_scores,
                                     workspace, workspace_bytes, stream)
+
+
+def dcp_topk_merge_shards(shard_scores, shard_ids, T, dcp, K, row_starts, out_ids, out_scores,
+                          stream=None) -> int:
+    return library().dcp_topk_merge_shards(shard_scores, shard_ids, T, dcp, K, row_starts, out_ids,
+                                           out_scores, stream)
 
 
 def dcp_topk_merge_workspace_size(T, dcp, K):
@@ -223,6 +234,57 @@ def merge(scores, ids, row_starts=None, out_ids=None, out_scores=None, stream=No
         _stream_handle(stream, dev)))
     if st != DCP_OK:
         raise DcpError(st, "dcp_topk_merge")
+    return out_ids, out_scores
+
+
+def merge_shards(shard_scores, shard_ids, row_starts=None, out_ids=None, out_scores=None,
+                 stream=None, pointer_arrays=None):
+    """Global top-K of shards held in separate tensors (read in place).
+
+    shard_scores: sequence of dcp float32 (T, K) CUDA tensors; shard_ids: the
+    matching int32 (T, K) tensors.  pointer_arrays: optional pair of int64
+    CUDA tensors of length dcp to hold the shards' addresses (filled here);
+    by default they are allocated per call.  The arrays are read on the
+    device, so they must outlive the stream's use of the call.  Returns
+    (out_ids int32 (T, K), out_scores float32 (T, K)).
+    """
+    torch = _torch()
+    dcp = len(shard_scores)
+    if dcp < 1 or len(shard_ids) != dcp:
+        raise ValueError("need the same number (>= 1) of score and id shards")
+    _check(shard_scores[0], "shard_scores[0]", torch.float32, None)
+    dev = shard_scores[0].get_device()
+    T, K = shard_scores[0].shape
+    for r in range(dcp):
+        _check(shard_scores[r], f"shard_scores[{r}]", torch.float32, dev)
+        _check(shard_ids[r], f"shard_ids[{r}]", torch.int32, dev)
+        if shard_scores[r].shape != (T, K) or shard_ids[r].shape != (T, K):
+            raise ValueError("every shard must be (T, K)")
+    if row_starts is not None:
+        _check(row_starts, "row_starts", torch.int32, dev)
+        if row_starts.shape != (T,):
+            raise ValueError("row_starts must be (T,)")
+    if out_ids is None:
+        out_ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    if out_scores is None:
+        out_scores = torch.empty((T, K), dtype=torch.float32, device=dev)
+    _check(out_ids, "out_ids", torch.int32, dev)
+    _check(out_scores, "out_scores", torch.float32, dev)
+    if out_ids.shape != (T, K) or out_scores.shape != (T, K):
+        raise ValueError("outputs must be (T, K)")
+    if pointer_arrays is None:
+        ps = torch.tensor([x.data_ptr() for x in shard_scores], dtype=torch.int64).to(dev)
+        pi = torch.tensor([x.data_ptr() for x in shard_ids], dtype=torch.int64).to(dev)
+    else:
+        ps, pi = pointer_arrays
+        ps.copy_(torch.tensor([x.data_ptr() for x in shard_scores], dtype=torch.int64))
+        pi.copy_(torch.tensor([x.data_ptr() for x in shard_ids], dtype=torch.int64))
+    st = _on_device(dev, lambda: library().dcp_topk_merge_shards(
+        ps.data_ptr(), pi.data_ptr(), T, dcp, K,
+        None if row_starts is None else row_starts.data_ptr(),
+        out_ids.data_ptr(), out_scores.data_ptr(), _stream_handle(stream, dev)))
+    if st != DCP_OK:
+        raise DcpError(st, "dcp_topk_merge_shards")
     return out_ids, out_scores
 
 

@@ -21,16 +21,62 @@ namespace dcp {
 // does; rows are independent, so this only fixes the order of the walk.
 constexpr int kChunkRows = 1024;
 
-struct MergeSource {
-  const float* scores;
+// The candidates of a merge.  Shard r's row t holds K scores and K ids:
+// - rank-major layout (Indirect = false): one (dcp, T, K) buffer each, shard
+//   r of row t at (r*T + t)*K, as the gather of "Reserve the sparse indexer's
+//   DCP top-k merge scratch through the workspace manager" (Purpose) leaves
+//   them;
+// - separate shards (Indirect = true): a device array of dcp pointers to
+//   (T, K) row-major shards, row t of shard r at shard[r] + t*K, the shards
+//   read where they lie ("[DCP][Performance] Add Shared-DCP peer-addressable
+//   decode data paths", Summary: the Top-K consumer reads owner-local and
+//   peer shards through views instead of an inbox).
+// Candidate index i = r*K + k in both.
+template <bool Indirect>
+struct MergeSourceT {
+  const float* scores;               // rank-major layout
   const int32_t* ids;
+  const float* const* shard_scores;  // separate shards: device arrays of dcp pointers
+  const int32_t* const* shard_ids;
   const int32_t* row_starts;
   int T, dcp, K;
   bool vec4;
+  static constexpr bool kIndirect = Indirect;
+  static constexpr bool kMerge = true;
+
+  // Row t of shard r.
+  __device__ const float* score_row(int t, int r) const {
+    if constexpr (Indirect)
+      return reinterpret_cast<const float*>(
+                 __ldg(reinterpret_cast<const unsigned long long*>(shard_scores) + r)) +
+             (size_t)t * (size_t)K;
+    else
+      return scores + ((size_t)r * T + t) * (size_t)K;
+  }
+  __device__ const int32_t* id_row(int t, int r) const {
+    if constexpr (Indirect)
+      return reinterpret_cast<const int32_t*>(
+                 __ldg(reinterpret_cast<const unsigned long long*>(shard_ids) + r)) +
+             (size_t)t * (size_t)K;
+    else
+      return ids + ((size_t)r * T + t) * (size_t)K;
+  }
+  // Whether every shard pointer allows the 16-byte copies of the fast paths
+  // (separate shards: the host cannot see the device-resident pointers).
+  __device__ bool shards_aligned() const {
+    if constexpr (Indirect) {
+      uintptr_t bits = 0;
+      for (int r = 0; r < dcp; ++r)
+        bits |= (uintptr_t)score_row(0, r) | (uintptr_t)id_row(0, r);
+      return (bits & 15u) == 0;
+    } else {
+      return true;
+    }
+  }
 
   __device__ int count() const { return dcp * K; }
 
-  // Candidates of row t, rank-major: index i = r*K + k.
+  // Candidates of row t: index i = r*K + k.
   __device__ void stage(int t, uint32_t* skey, uint32_t* sinv) const {
     const int n = dcp * K;
     if (vec4) {
@@ -38,9 +84,8 @@ struct MergeSource {
       for (int q = threadIdx.x; q < (n >> 2); q += kThreads) {
         const int r = q / k4;
         const int kk = (q - r * k4) << 2;
-        const size_t off = ((size_t)r * T + t) * (size_t)K + kk;
-        const uint4 sb = __ldg(reinterpret_cast<const uint4*>(scores + off));
-        const int4 ib = __ldg(reinterpret_cast<const int4*>(ids + off));
+        const uint4 sb = __ldg(reinterpret_cast<const uint4*>(score_row(t, r) + kk));
+        const int4 ib = __ldg(reinterpret_cast<const int4*>(id_row(t, r) + kk));
         const int i = r * K + kk;
         *reinterpret_cast<uint4*>(skey + i) =
             make_uint4(score_key(sb.x), score_key(sb.y), score_key(sb.z), score_key(sb.w));
@@ -51,16 +96,15 @@ struct MergeSource {
       for (int i = threadIdx.x; i < n; i += kThreads) {
         const int r = i / K;
         const int k = i - r * K;
-        const size_t off = ((size_t)r * T + t) * (size_t)K + k;
-        skey[i] = score_key(__float_as_uint(__ldg(scores + off)));
-        sinv[i] = ~(uint32_t)__ldg(ids + off);
+        skey[i] = score_key(__float_as_uint(__ldg(score_row(t, r) + k)));
+        sinv[i] = ~(uint32_t)__ldg(id_row(t, r) + k);
       }
     }
   }
 
   // Fast path staging: the row's scores and its ids, each as dcp 16-byte
-  // copies straight from the rank-major layout (needs K % 4 == 0 and
-  // 16-byte aligned bases), completing on separate barriers.
+  // copies straight from the shards (needs K % 4 == 0 and 16-byte aligned
+  // shards), completing on separate barriers.
   static constexpr bool kStagesIds = true;
   // ids are arbitrary: their order is not the candidates' order
   __device__ bool index_ordered() const { return false; }
@@ -71,18 +115,14 @@ struct MergeSource {
   __device__ void issue_scores(int t, uint32_t* dst, unsigned long long* bar) const {
     const uint32_t seg = (uint32_t)K * 4u;
     mbar_expect_tx(bar, (uint32_t)dcp * seg);
-    const size_t stride = (size_t)T * (size_t)K;
-    const float* sp = scores + (size_t)t * (size_t)K;
-    for (int r = 0; r < dcp; ++r, sp += stride) tma_load_1d(dst + r * K, sp, seg, bar);
+    for (int r = 0; r < dcp; ++r) tma_load_1d(dst + r * K, score_row(t, r), seg, bar);
   }
 
   // One thread: the same for row t's ids.
   __device__ void issue_ids(int t, uint32_t* dst, unsigned long long* bar) const {
     const uint32_t seg = (uint32_t)K * 4u;
     mbar_expect_tx(bar, (uint32_t)dcp * seg);
-    const size_t stride = (size_t)T * (size_t)K;
-    const int32_t* ip = ids + (size_t)t * (size_t)K;
-    for (int r = 0; r < dcp; ++r, ip += stride) tma_load_1d(dst + r * K, ip, seg, bar);
+    for (int r = 0; r < dcp; ++r) tma_load_1d(dst + r * K, id_row(t, r), seg, bar);
   }
 
   // Inverted ids of staged candidates 4c .. 4c+3 (staged ids at `staged`).
@@ -94,33 +134,30 @@ struct MergeSource {
   // Candidate i of row t read from global memory (the fallback path).
   __device__ uint32_t key_global(int t, int i) const {
     const int r = i / K;
-    return score_key(__float_as_uint(__ldg(scores + ((size_t)r * T + t) * (size_t)K + (i - r * K))));
+    return score_key(__float_as_uint(__ldg(score_row(t, r) + (i - r * K))));
   }
   __device__ uint32_t inv_global(int t, int i) const {
     const int r = i / K;
-    return ~(uint32_t)__ldg(ids + ((size_t)r * T + t) * (size_t)K + (i - r * K));
+    return ~(uint32_t)__ldg(id_row(t, r) + (i - r * K));
   }
   // Score keys of candidates 4c .. 4c+3 of row t (one shard: K % 4 == 0).
   __device__ uint4 key4_global(int t, int c) const {
     const int i = 4 * c, r = i / K;
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(scores + ((size_t)r * T + t) * (size_t)K +
-                                                         (i - r * K)));
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(score_row(t, r) + (i - r * K)));
     return make_uint4(score_key(w.x), score_key(w.y), score_key(w.z), score_key(w.w));
   }
 
   // Ids of candidates 4c .. 4c+3 of row t (one shard: K % 4 == 0).
   __device__ uint4 ids4_global(int t, int c) const {
     const int i = 4 * c, r = i / K;
-    return __ldg(reinterpret_cast<const uint4*>(ids + ((size_t)r * T + t) * (size_t)K + (i - r * K)));
+    return __ldg(reinterpret_cast<const uint4*>(id_row(t, r) + (i - r * K)));
   }
 
   // One thread: pulls row t's scores and ids of every shard into L2.
   __device__ void prefetch_row(int t) const {
-    const size_t stride = (size_t)T * (size_t)K;
-    const size_t off = (size_t)t * (size_t)K;
     for (int r = 0; r < dcp; ++r) {
-      prefetch_l2(scores + off + r * stride, (uint32_t)K * 4u);
-      prefetch_l2(ids + off + r * stride, (uint32_t)K * 4u);
+      prefetch_l2(score_row(t, r), (uint32_t)K * 4u);
+      prefetch_l2(id_row(t, r), (uint32_t)K * 4u);
     }
   }
 
@@ -141,6 +178,8 @@ struct MergeSource {
     return (int32_t)(id + rs);
   }
 };
+using MergeSource = MergeSourceT<false>;
+using ShardsSource = MergeSourceT<true>;
 
 // Column c of one rank's shard is candidate c (ordered by ~c: the global id
 // grows with the column in both shard layouts); its global id is
@@ -176,6 +215,9 @@ struct LocalSource {
 
   // Ids are column numbers: only the logits are staged.
   static constexpr bool kStagesIds = false;
+  static constexpr bool kIndirect = false;
+  static constexpr bool kMerge = false;
+  __device__ bool shards_aligned() const { return true; }
   __device__ bool index_ordered() const { return true; }  // ids grow with the column
   __host__ __device__ int score_words() const { return L; }
   __host__ __device__ int ids_words() const { return 0; }
@@ -246,6 +288,9 @@ struct FusedSource {
 
   // Ids are r*L + c: only the logits are staged.
   static constexpr bool kStagesIds = false;
+  static constexpr bool kIndirect = false;
+  static constexpr bool kMerge = false;
+  __device__ bool shards_aligned() const { return true; }
   // ids grow with the candidate index only in the contiguous layout
   __device__ bool index_ordered() const { return !interleaved; }
   __host__ __device__ int score_words() const { return dcp * L; }
@@ -410,12 +455,17 @@ static cudaError_t device_info(DeviceInfo** out) {
     if (e != cudaSuccess) return e;
     const int smem = d.max_smem_optin;
     if ((e = allow_max_smem(topk_rows_kernel<MergeSource>, smem)) != cudaSuccess) return e;
+    if ((e = allow_max_smem(topk_rows_kernel<ShardsSource>, smem)) != cudaSuccess) return e;
     if ((e = allow_max_smem(topk_rows_kernel<LocalSource>, smem)) != cudaSuccess) return e;
     if ((e = allow_max_smem(topk_rows_kernel<FusedSource>, smem)) != cudaSuccess) return e;
     if ((e = allow_stream_kernels<MergeSource>(smem)) != cudaSuccess) return e;
+    if ((e = allow_stream_kernels<ShardsSource>(smem)) != cudaSuccess) return e;
     if ((e = allow_stream_kernels<LocalSource>(smem)) != cudaSuccess) return e;
     if ((e = allow_stream_kernels<FusedSource>(smem)) != cudaSuccess) return e;
     if ((e = allow_max_smem(merge_rows_kernel<MergeSource>, (int)sizeof(RowsShared))) !=
+        cudaSuccess)
+      return e;
+    if ((e = allow_max_smem(merge_rows_kernel<ShardsSource>, (int)sizeof(RowsShared))) !=
         cudaSuccess)
       return e;
     if ((e = status_word(&d.status)) != cudaSuccess) return e;
@@ -487,12 +537,12 @@ static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out
                          smem <= (size_t)d->max_smem_optin;
   const int grid1 = T < d->sms ? T : d->sms;
   cudaError_t e;
-  if constexpr (std::is_same<Source, MergeSource>::value) {
+  if constexpr (Source::kMerge) {
     if (src.vec4 && K == kRowsK && n <= kRowsMaxN && T > d->sms &&
         sizeof(RowsShared) <= (size_t)d->max_smem_optin) {
       const int grid = T < 4 * d->sms ? T : 4 * d->sms;
-      e = launch_serialized(merge_rows_kernel<MergeSource>, grid, kRowsNT, sizeof(RowsShared),
-                            stream, src, T, out_scores, out_ids);
+      e = launch_serialized(merge_rows_kernel<Source>, grid, kRowsNT, sizeof(RowsShared), stream,
+                            src, T, out_scores, out_ids, d->status);
       return e == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
     }
   }
@@ -513,11 +563,16 @@ static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out
     const size_t gsmem = row_smem_bytes(n, K);
     if (gsmem > (size_t)d->max_smem_optin) return DCP_ERR_UNSUPPORTED;
     const int grid = T < d->sms ? T : d->sms;
-    e = launch_serialized(topk_rows_kernel<Source>, grid, kThreads, gsmem, stream, src, T, K,
+    // separate shards: scalar loads here, since this kernel does not check
+    // the shards' alignment
+    Source gsrc = src;
+    if constexpr (Source::kIndirect) gsrc.vec4 = false;
+    e = launch_serialized(topk_rows_kernel<Source>, grid, kThreads, gsmem, stream, gsrc, T, K,
                           out_scores, out_ids);
   }
-  if (e != cudaSuccess) return DCP_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+  // the launch's own status only: an error left on the thread by unrelated
+  // work is neither reported here nor cleared
+  return e == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
 }
 
 }  // namespace dcp
@@ -540,8 +595,35 @@ dcp_status dcp_topk_merge(const float* scores, const int32_t* ids, int T, int dc
   if (K > DCP_MAX_K || (long long)dcp_ * K > DCP_MAX_CANDIDATES) return DCP_ERR_UNSUPPORTED;
   if (T == 0) return DCP_OK;
   if (!scores || !ids || !out_ids || !out_scores) return DCP_ERR_INVALID;
-  dcp::MergeSource src{scores, ids, row_starts, T, dcp_, K,
+  dcp::MergeSource src{scores, ids, nullptr, nullptr, row_starts, T, dcp_, K,
                        (K % 4) == 0 && dcp::aligned16(scores) && dcp::aligned16(ids)};
+  return dcp::launch_rows(src, T, dcp_ * K, K, out_scores, out_ids, (cudaStream_t)stream);
+}
+
+// Whether `p` is memory the device can read (device, managed, or mapped
+// host memory): a host-only pointer array would fault the kernel.
+static bool device_readable(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clears the error this query itself raised
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+         (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr);
+}
+
+dcp_status dcp_topk_merge_shards(const float* const* shard_scores, const int32_t* const* shard_ids,
+                                 int T, int dcp_, int K, const int32_t* row_starts,
+                                 int32_t* out_ids, float* out_scores, dcp_stream_t stream) {
+  if (T < 0 || dcp_ < 1 || K < 1) return DCP_ERR_INVALID;
+  if (K > DCP_MAX_K || (long long)dcp_ * K > DCP_MAX_CANDIDATES) return DCP_ERR_UNSUPPORTED;
+  if (T == 0) return DCP_OK;
+  if (!shard_scores || !shard_ids || !out_ids || !out_scores) return DCP_ERR_INVALID;
+  if (!device_readable(shard_scores) || !device_readable(shard_ids)) return DCP_ERR_INVALID;
+  // 16-byte paths when K allows them; the shard pointers themselves are
+  // checked on the device (DCP_DEVICE_BAD_SHARD_ALIGNMENT)
+  dcp::ShardsSource src{nullptr, nullptr, shard_scores, shard_ids, row_starts, T, dcp_, K,
+                        (K % 4) == 0};
   return dcp::launch_rows(src, T, dcp_ * K, K, out_scores, out_ids, (cudaStream_t)stream);
 }
 
@@ -620,8 +702,14 @@ dcp_status dcp_topk_device_status(unsigned int* status) {
 dcp_status dcp_topk_selftest_wait_timeout(unsigned int wait_cycles, dcp_stream_t stream) {
   unsigned int* word = nullptr;
   if (dcp::status_word(&word) != cudaSuccess) return DCP_ERR_CUDA;
-  dcp::wait_timeout_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(wait_cycles, word);
-  return cudaGetLastError() == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1u);
+  cfg.blockDim = dim3(32u);
+  cfg.stream = (cudaStream_t)stream;
+  const unsigned long long limit = wait_cycles;
+  return cudaLaunchKernelEx(&cfg, dcp::wait_timeout_selftest_kernel, limit, word) == cudaSuccess
+             ? DCP_OK
+             : DCP_ERR_CUDA;
 }
 
 const char* dcp_status_string(dcp_status status) {

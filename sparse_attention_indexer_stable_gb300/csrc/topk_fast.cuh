@@ -63,6 +63,7 @@ constexpr uint32_t kBigBucket = 255;          // a larger bucket starting before
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr unsigned long long kStageWaitLimit = 1ull << 31;  // cycles (about 1 s) to wait for a row's copy
 constexpr uint32_t kStatusCopyTimeout = 1u;     // device status bit: a staging copy timed out
+constexpr uint32_t kStatusBadShardAlignment = 2u;  // device status bit: a shard not 16-byte aligned
 
 // Per-row sizes for a CTA of NT threads selecting up to KMAX winners.
 // - The 512-thread CTAs walk many rows two to an SM: their L1 bins are the
@@ -178,6 +179,22 @@ __device__ __forceinline__ void tma_load_1d(void* smem_dst, const void* gmem_src
           smem_u32(smem_dst)),
       "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Marks the rows t, t + G, ... < T of a CTA that stops after a copy timed
+// out: every slot gets id DCP_ID_UNWRITTEN and a NaN score, so that a
+// caller who does not check the device status cannot mistake stale memory
+// for a result.  Every thread of the CTA calls it.
+__device__ __noinline__ void mark_rows_unwritten(float* out_scores, int32_t* out_ids, int t, int T,
+                                                 int G, int K) {
+  for (; t < T; t += G) {
+    float* os = out_scores + (size_t)t * (size_t)K;
+    int32_t* oi = out_ids + (size_t)t * (size_t)K;
+    for (int j = threadIdx.x; j < K; j += blockDim.x) {
+      os[j] = __uint_as_float(0x7FFFFFFFu);  // NaN
+      oi[j] = INT32_MIN;                      // DCP_ID_UNWRITTEN
+    }
+  }
 }
 
 // Waits for phase `parity` of `bar` to complete, giving up once `limit`
@@ -542,6 +559,14 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   }
   __syncthreads();
   grid_dependency_wait();  // every thread, before its first global access
+  if constexpr (Source::kIndirect) {
+    // separate shards: their 16-byte alignment is only visible here
+    if (!__syncthreads_and(tid != 0 || src.shards_aligned())) {
+      if (tid == 0) atomicOr(status, kStatusBadShardAlignment);
+      mark_rows_unwritten(out_scores, out_ids, t, T, G, K);
+      return;
+    }
+  }
   if (tid == 0) {
     if (t < T) {
       src.issue_scores(t, stage, &s.stage_bar);
@@ -553,11 +578,14 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     const bool staged = mbar_wait_bounded(&s.stage_bar, k & 1u, kStageWaitLimit);
     // the row is staged (or its copy timed out) and the previous row's state reset
     if (__syncthreads_or(!staged)) {
-      // Report the timeout and stop this CTA; first give the copies a last,
-      // bounded chance to land so no copy is left writing into shared memory.
+      // Report the timeout, mark this CTA's rows unwritten and stop; first
+      // give the copies a last, bounded chance to land.  If one never lands
+      // the CTA still exits (nothing waits forever); such a copy could only
+      // write into this CTA's shared memory.
       if (tid == 0) atomicOr(status, kStatusCopyTimeout);
       mbar_wait_bounded(&s.stage_bar, k & 1u, kStageWaitLimit);
       if constexpr (Source::kStagesIds) mbar_wait_bounded(&s.ids_bar, k & 1u, kStageWaitLimit);
+      mark_rows_unwritten(out_scores, out_ids, t, T, G, K);
       return;
     }
     // The copy of the next row's scores into the stage starts as soon as this
@@ -649,6 +677,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         if (tid == 0) atomicOr(status, kStatusCopyTimeout);
         mbar_wait_bounded(&s.ids_bar, k & 1u, kStageWaitLimit);
         if (next_issued) mbar_wait_bounded(&s.stage_bar, (k + 1u) & 1u, kStageWaitLimit);
+        mark_rows_unwritten(out_scores, out_ids, t, T, G, K);
         return;
       }
     } else {

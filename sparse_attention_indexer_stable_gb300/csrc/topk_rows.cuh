@@ -197,7 +197,7 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
 template <class Source>
 __global__ void __launch_bounds__(kRowsNT, 4)
     merge_rows_kernel(Source src, int T, float* __restrict__ out_scores,
-                      int32_t* __restrict__ out_ids) {
+                      int32_t* __restrict__ out_ids, unsigned int* __restrict__ status) {
   constexpr int NT = kRowsNT;
   constexpr int kWarpsT = NT / 32;          // 8
   constexpr int kVec = kRowsMaxN / 4 / NT;  // 16-byte chunks per thread: 8
@@ -239,17 +239,34 @@ __global__ void __launch_bounds__(kRowsNT, 4)
   const int G = (int)gridDim.x;
   int t = (int)blockIdx.x;
   grid_dependency_wait();  // every thread, before its first global access
+  if constexpr (Source::kIndirect) {
+    // separate shards: their 16-byte alignment is only visible here
+    if (!__syncthreads_and(tid != 0 || src.shards_aligned())) {
+      if (tid == 0) atomicOr(status, kStatusBadShardAlignment);
+      mark_rows_unwritten(out_scores, out_ids, t, T, G, K);
+      return;
+    }
+  }
   if (tid == 0 && t < T) src.prefetch_row(t);
 
   for (; t < T; t += G) {
-    const float* srow = src.scores + (size_t)t * K;
-    const int32_t* irow = src.ids + (size_t)t * K;
+    // this thread's 16-byte chunk v of row t: shard v/2, chunk tid + 256*(v%2)
+    auto score_chunk = [&](int v) -> const float* {
+      if constexpr (Source::kIndirect)
+        return src.score_row(t, v >> 1) + 4 * (tid + NT * (v & 1));
+      else
+        return src.scores + (size_t)t * K + (size_t)(v >> 1) * shard_stride + 4 * (tid + NT * (v & 1));
+    };
+    auto id_chunk = [&](int v) -> const int32_t* {
+      if constexpr (Source::kIndirect)
+        return src.id_row(t, v >> 1) + 4 * (tid + NT * (v & 1));
+      else
+        return src.ids + (size_t)t * K + (size_t)(v >> 1) * shard_stride + 4 * (tid + NT * (v & 1));
+    };
     uint4 w[kVec];
 #pragma unroll
     for (int v = 0; v < kVec; ++v)
-      w[v] = (tid + v * NT) < n4
-                 ? ldg4(srow + (size_t)(v >> 1) * shard_stride + 4 * (tid + NT * (v & 1)))
-                 : make_uint4(0u, 0u, 0u, 0u);
+      w[v] = (tid + v * NT) < n4 ? ldg4(score_chunk(v)) : make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();  // the previous row's shared state is reset
 
     // ---- L1: histogram of the score keys' top 12 bits ----------------------
@@ -378,7 +395,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
 #pragma unroll
       for (int v = 0; v < kVec; ++v) {
         if ((tid + v * NT) < n4) {
-          const uint4 iv = ldg4(irow + (size_t)(v >> 1) * shard_stride + 4 * (tid + NT * (v & 1)));
+          const uint4 iv = ldg4(id_chunk(v));
           const uint32_t us[4] = {~iv.x, ~iv.y, ~iv.z, ~iv.w};
           ior |= us[0] | us[1] | us[2] | us[3];
           if (has_pad)

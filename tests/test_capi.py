@@ -121,3 +121,29 @@ def test_layout_names():
     assert dk._layout("interleaved") == dk.DCP_IDS_INTERLEAVED
     with pytest.raises(ValueError):
         dk._layout("striped")
+
+
+@pytest.mark.parametrize("args,want", [
+    ((FAKE, FAKE, -1, 4, 16, None, FAKE, FAKE), dk.DCP_ERR_INVALID),
+    ((FAKE, FAKE, 4, 0, 16, None, FAKE, FAKE), dk.DCP_ERR_INVALID),
+    ((FAKE, FAKE, 4, 4, 0, None, FAKE, FAKE), dk.DCP_ERR_INVALID),
+    ((None, FAKE, 4, 4, 16, None, FAKE, FAKE), dk.DCP_ERR_INVALID),
+    ((FAKE, None, 4, 4, 16, None, FAKE, FAKE), dk.DCP_ERR_INVALID),
+    ((FAKE, FAKE, 4, 4, 16, None, None, FAKE), dk.DCP_ERR_INVALID),
+    ((FAKE, FAKE, 4, 4, 16, None, FAKE, None), dk.DCP_ERR_INVALID),
+    # pointer arrays the device cannot read (here: not memory of any device)
+    ((FAKE, FAKE, 4, 4, 16, None, FAKE, FAKE), dk.DCP_ERR_INVALID),
+    ((FAKE, FAKE, 4, 1, 4097, None, FAKE, FAKE), dk.DCP_ERR_UNSUPPORTED),
+    ((FAKE, FAKE, 4, 5, 4096, None, FAKE, FAKE), dk.DCP_ERR_UNSUPPORTED),
+    ((None, None, 0, 4, 16, None, None, None), dk.DCP_OK),  # T == 0 is a no-op
+])
+def test_merge_shards_argument_errors(args, want):
+    assert dk.dcp_topk_merge_shards(*args, None) == want
+
+
+def test_merge_shards_rejects_host_pointer_arrays():
+    """Pointer arrays in ordinary host memory would fault the kernel: the
+    call refuses them before launching anything."""
+    arr = (ctypes.c_uint64 * 4)(FAKE, FAKE, FAKE, FAKE)
+    p = ctypes.addressof(arr)
+    assert dk.dcp_topk_merge_shards(p, p, 2, 4, 16, None, FAKE, FAKE, None) == dk.DCP_ERR_INVALID
