@@ -36,21 +36,34 @@ def _inputs():
     return files
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+# The race-check build: the same library compiled with -DDCP_DEBUG_POISON
+# (odd warps delayed after every barrier, shared state overwritten with
+# garbage before every reset, indices from shared state clamped), for the
+# barrier tests only; it exports the same C ABI.
+POISON_LIB_PATH = os.path.join(OUT_DIR, "libdcp_topk_racecheck.so")
+POISON_FLAGS = ("-DDCP_DEBUG_POISON",)
+
+
+def is_stale(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, extra_flags=(), path: str = LIB_PATH) -> str:
     """Compile the library if missing or older than its sources; returns its path."""
-    if not force and not is_stale():
-        return LIB_PATH
+    if not force and not is_stale(path):
+        return path
     os.makedirs(OUT_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".{os.getpid()}.tmp"
+    tmp = path + f".{os.getpid()}.tmp"
     cmd = [_nvcc(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "--shared",
            "-Xcompiler", "-fPIC", "-I", INCLUDE, "-o", tmp, *sources(), *extra_flags]
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, path)
+    return path
+
+
+def build_race_check(force: bool = False) -> str:
+    """The race-check build (see POISON_LIB_PATH); returns its path."""
+    return build(force, POISON_FLAGS, POISON_LIB_PATH)

@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int t = cs + (((b - cs) % grid) + grid) % grid;
     for (; t < ce; t += grid) {
       src.stage(t, skey, sinv);
-      __syncthreads();
+      row_sync();
       select_sort_row<kThreads>(s, n, ksel, win, n_pow2, [&](int i) { return skey[i]; },
                                 [&](int i) { return sinv[i]; });
       float* os = out_scores + (size_t)t * (size_t)K;
@@ -385,15 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // The next row's staging overwrites skey/sinv/win.
-      __syncthreads();
+      row_sync();
+      if constexpr (kPoisonBuild) {
+        dbg_poison<kThreads>(smem_raw, (int)(row_smem_bytes(n, K) / 4));
+        __syncthreads();
+      }
     }
   }
 }
 
-// Device status word: kernels set bits here on failures they detect (a
-// staging copy that never completed); read and cleared by
-// dcp_topk_device_status.
-__device__ unsigned int g_device_status;
 
 static cudaError_t status_word(unsigned int** out) {
   return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_device_status);

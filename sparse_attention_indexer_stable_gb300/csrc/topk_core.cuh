@@ -29,6 +29,71 @@ constexpr int kThreads = 1024;
 constexpr int kMaxWarps = 32;
 constexpr int kHistBins = 2048;
 
+// Device status word: kernels set bits here on failures they detect (a
+// staging copy that never completed, a misaligned shard, a clamped index in
+// the race-check build); read and cleared by dcp_topk_device_status.
+__device__ unsigned int g_device_status;
+constexpr uint32_t kStatusPoisonClamp = 4u;  // race-check build: an index from shared state clamped
+
+// ---- Race-check build (compiled with -DDCP_DEBUG_POISON) -------------------
+// The race the first page's review reports: shared state reset while a late
+// warp had not yet read it (a threshold loaded, then zeroed with no barrier
+// in between; late warps read 0 and drop every tied candidate).  Whether such
+// a missing barrier shows up depends on warp timing.  The race-check build
+// removes the dependence:
+//  - after every barrier of the row loops the odd warps wait a bounded while,
+//    so at every phase boundary some warps are the late readers;
+//  - every reset of shared state is preceded by an overwrite with garbage and
+//    a barrier, so a reader that no barrier orders before the reset reads
+//    garbage, not a value that might happen to be right;
+//  - indices taken from shared state are clamped into their arrays and the
+//    clamp recorded (kStatusPoisonClamp), so reading garbage cannot fault.
+// A missing barrier then gives a wrong answer or a status bit, which the
+// parity tests catch.  Without the macro all of this compiles to nothing.
+#ifdef DCP_DEBUG_POISON
+constexpr bool kPoisonBuild = true;
+#else
+constexpr bool kPoisonBuild = false;
+#endif
+
+// Race-check build: the odd warps wait about 3000 cycles (a bounded delay).
+__device__ __forceinline__ void dbg_skew() {
+  if constexpr (kPoisonBuild) {
+    if ((threadIdx.x >> 5) & 1u) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < 3000) {
+      }
+    }
+  }
+}
+
+// __syncthreads(), then the race-check build's skew.
+__device__ __forceinline__ void row_sync() {
+  __syncthreads();
+  dbg_skew();
+}
+
+// Race-check build: `words` 32-bit words at p overwritten with garbage by
+// the CTA's NT threads.
+template <int NT>
+__device__ __forceinline__ void dbg_poison(void* p, int words) {
+  if constexpr (kPoisonBuild) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(p);
+    for (int i = threadIdx.x; i < words; i += NT) w[i] = 0xA5A5A5A5u ^ ((uint32_t)i * 0x9E3779B9u);
+  }
+}
+
+// Race-check build: i clamped into [0, n), the clamp recorded.
+__device__ __forceinline__ uint32_t dbg_clamp(uint32_t i, uint32_t n) {
+  if constexpr (kPoisonBuild) {
+    if (i >= n) {
+      atomicOr(&g_device_status, kStatusPoisonClamp);
+      return n - 1u;
+    }
+  }
+  return i;
+}
+
 // Order-preserving map of fp32 bits to u32: unsigned order of the result is
 // float order, with -0.0 just below +0.0 and NaNs outside the finite range.
 // Negative values have every bit inverted, the others only the sign bit.
@@ -85,13 +150,13 @@ __device__ __forceinline__ void find_threshold_digit(SelectShared& s, int nbins,
   }
   const uint32_t incl = warp_inclusive_scan(local);
   if (lane == 31) s.warp_sum[warp] = incl;
-  __syncthreads();
+  row_sync();
   if (warp == 0) {
     const uint32_t w = lane < NT / 32 ? s.warp_sum[lane] : 0u;
     const uint32_t wi = warp_inclusive_scan(w);
     s.warp_off[lane] = wi - w;
   }
-  __syncthreads();
+  row_sync();
   uint32_t above = s.warp_off[warp] + incl - local;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
@@ -128,15 +193,19 @@ __device__ __forceinline__ RadixResult radix_select(SelectShared& s, int n, uint
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const int nbins = pass == 2 ? 1024 : 2048;
     const uint32_t dmask = (uint32_t)nbins - 1u;
+    if constexpr (kPoisonBuild) {
+      dbg_poison<NT>(&s, (int)(sizeof(SelectShared) / 4));
+      __syncthreads();
+    }
     for (int b = tid; b < nbins; b += NT) s.hist[b] = 0u;
-    __syncthreads();
+    row_sync();
     for (int i = tid; i < n; i += NT) {
       uint32_t v;
       if (value(i, v) && (v & r.mask) == r.prefix) atomicAdd(&s.hist[(v >> shift) & dmask], 1u);
     }
-    __syncthreads();
+    row_sync();
     find_threshold_digit<NT>(s, nbins, r.need);
-    __syncthreads();
+    row_sync();
     const uint32_t d = s.found_digit, above = s.found_above, cnt = s.found_count;
     r.need -= above;
     r.prefix |= d << shift;
@@ -144,7 +213,7 @@ __device__ __forceinline__ RadixResult radix_select(SelectShared& s, int n, uint
     r.count = cnt;
     // Every thread has now read found_* and the histogram; only after this
     // barrier may the next pass (or the caller) reset them.
-    __syncthreads();
+    row_sync();
     if (cnt == r.need) break;
   }
   return r;
@@ -166,7 +235,7 @@ __device__ __forceinline__ void bitonic_sort_desc(unsigned long long* a, int n_p
           a[hi] = x;
         }
       }
-      __syncthreads();
+      row_sync();
     }
   }
 }
@@ -204,7 +273,7 @@ __device__ __forceinline__ void select_sort_row(SelectShared& s, int n, int ksel
     s.win_count = 0u;
     s.dup_claim = 0u;
   }
-  __syncthreads();
+  row_sync();
 
   // 3. Compaction of the winners (order is irrelevant: the sort below fixes
   //    it, and candidates with equal 64-bit keys are identical).
@@ -238,7 +307,7 @@ __device__ __forceinline__ void select_sort_row(SelectShared& s, int n, int ksel
     }
   }
   for (int j = ksel + tid; j < n_pow2; j += NT) win[j] = 0ull;
-  __syncthreads();
+  row_sync();
 
   // 4. Final order.
   bitonic_sort_desc<NT>(win, n_pow2);

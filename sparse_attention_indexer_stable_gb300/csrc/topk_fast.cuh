@@ -272,12 +272,12 @@ __device__ __forceinline__ void find_digit_desc(const uint32_t* hist, uint32_t n
   for (int e = 0; e < kPer; ++e) local += h[e];
   const uint32_t incl = warp_inclusive_scan(local);
   if (lane == 31) wa[warp] = incl;
-  __syncthreads();
+  row_sync();
   if (warp == 0) {
     const uint32_t w = lane < NT / 32 ? wa[lane] : 0u;
     wb[lane] = warp_inclusive_scan(w) - w;
   }
-  __syncthreads();
+  row_sync();
   uint32_t above = wb[warp] + incl - local;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
@@ -340,7 +340,7 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
   if constexpr (Source::kStagesIds) {
     if (s.b1 == Caps::kPadBin) {
       if (tid == 0) s.live_cursor = 0u;  // COMPACT's last use was barriers ago
-      __syncthreads();
+      row_sync();
       uint32_t npad = 0u;
 #pragma unroll 1
       for (int c0 = 0; c0 < n4; c0 += NT) {
@@ -375,13 +375,13 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
       }
       npad = __reduce_add_sync(0xFFFFFFFFu, npad);
       if (lane == 0 && npad != 0u) atomicAdd(&s.pad_n, npad);
-      __syncthreads();
+      row_sync();
       const uint32_t nreal = s.live_cursor;  // candidates above the padding key
       if (nreal < (uint32_t)ksel && nreal + s.pad_n >= (uint32_t)ksel) {
         int n_pow2 = 1;
         while (n_pow2 < (int)nreal) n_pow2 <<= 1;
         for (int j = (int)nreal + tid; j < n_pow2; j += NT) s.live[j] = 0ull;
-        __syncthreads();
+        row_sync();
         bitonic_sort_desc<NT>(s.live, n_pow2);
         nwin = tail = (int)nreal;
         sorted = true;
@@ -393,7 +393,7 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
         s.live_cursor = 0u;
         s.pad_n = 0u;  // here: the -inf candidates
       }
-      __syncthreads();
+      row_sync();
       uint32_t ninf = 0u;
 #pragma unroll 1
       for (int c0 = 0; c0 < n4; c0 += NT) {
@@ -428,7 +428,7 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
       }
       ninf = __reduce_add_sync(0xFFFFFFFFu, ninf);
       if (lane == 0 && ninf != 0u) atomicAdd(&s.pad_n, ninf);
-      __syncthreads();
+      row_sync();
       const uint32_t nf = s.live_cursor;  // candidates above -inf
       if (nf < (uint32_t)ksel && nf + s.pad_n >= (uint32_t)ksel) {
         // the first ksel - nf -inf candidates in index order take positions
@@ -449,7 +449,7 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
           const uint32_t cnt = __popc(f);
           const uint32_t incl = warp_inclusive_scan(cnt);
           if (lane == 31) s.wa[warp] = incl;
-          __syncthreads();
+          row_sync();
           const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
           const uint32_t wti = warp_inclusive_scan(wt);
           const uint32_t chunk = __shfl_sync(0xFFFFFFFFu, wti, kWarpsT - 1);
@@ -469,12 +469,12 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
             }
           }
           before += chunk;
-          __syncthreads();  // s.wa is rewritten by the next chunk
+          row_sync();  // s.wa is rewritten by the next chunk
         }
         int n_pow2 = 1;
         while (n_pow2 < (int)nf) n_pow2 <<= 1;
         for (int j = (int)nf + tid; j < n_pow2; j += NT) s.live[j] = 0ull;
-        __syncthreads();
+        row_sync();
         bitonic_sort_desc<NT>(s.live, n_pow2);
         nwin = (int)nf;
         sorted = true;
@@ -588,6 +588,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       mark_rows_unwritten(out_scores, out_ids, t, T, G, K);
       return;
     }
+    dbg_skew();
     // The copy of the next row's scores into the stage starts as soon as this
     // row's are consumed (after L1); its ids follow at the end of the row (the
     // aux region serves RANK until then) and are needed only by COMPACT.
@@ -617,7 +618,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     }
     raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & kLowMask);
     if (lane == 0 && raw_or) atomicOr(&s.stat_or[0], raw_or);
-    __syncthreads();
+    row_sync();
     // L1 was the last reader of the staged scores (the rest of the row works
     // from the keys in registers, the staged ids and, in the fallback, global
     // memory): stream the next row's scores in behind the rest of this one.
@@ -644,7 +645,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         incl = warp_inclusive_scan(local);
       }
       if (lane == 31) s.wa[warp] = incl;
-      __syncthreads();
+      row_sync();
       if (warp_busy) {
         // every warp scans the per-warp totals itself (no second barrier)
         const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
@@ -680,8 +681,9 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         mark_rows_unwritten(out_scores, out_ids, t, T, G, K);
         return;
       }
+      dbg_skew();
     } else {
-      __syncthreads();
+      row_sync();
     }
 
     const uint32_t b1 = s.b1;
@@ -698,16 +700,21 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         if ((tid + (j >> 2) * NT) < n4 && (keys[j] >> kL1Shift) == b1)
           atomicAdd(&s.fine[(keys[j] >> kRefShift) & 0x7FFu], 1u);
       }
-      __syncthreads();
+      row_sync();
       find_digit_desc<NT>(s.fine, (uint32_t)ksel - s.above_b1, s.wa, s.wb, s.found_digit,
                           s.found_above, s.found_count);
-      __syncthreads();
+      row_sync();
       live_from |= s.found_digit;
       const uint32_t nl = s.above_b1 + s.found_above + s.found_count;
+      if constexpr (kPoisonBuild) {
+        row_sync();
+        dbg_poison<NT>(s.fine, kHistBins);
+        __syncthreads();
+      }
       zero_words<NT>(s.fine, kHistBins);  // the refinement histogram: 2048 words of fine
-      __syncthreads();
+      row_sync();
       if (tid == 0) s.nlive = nl;
-      __syncthreads();
+      row_sync();
     }
     const int nlive = (int)s.nlive;
     bool fast = nlive <= kLiveMax;
@@ -728,7 +735,8 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       const uint32_t incl = warp_inclusive_scan(cnt);
       uint32_t base = 0u;
       if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
-      unsigned long long* dst = s.live + (__shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt);
+      unsigned long long* dst =
+          s.live + dbg_clamp(__shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt, kLiveMax + 1u - cnt);
       // OR / AND of the inverted ids around the live candidates (padding's
       // ~id of 0 left out: it is the smallest, so ordering on the varying
       // bits alone still puts it last)
@@ -754,7 +762,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         atomicAnd(&s.stat_and[1], iand);
       }
     }
-    __syncthreads();
+    row_sync();
 
     // ---- L2: fine bucket of every live candidate ---------------------------
     unsigned long long lkey[kLivePer];
@@ -795,12 +803,12 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
           }
           const uint32_t sub = w >= q ? (uint32_t)(y >> (w - q)) : (uint32_t)(y << (q - w));
           const uint32_t g = (tb >> 8) + ((1u << q) - 1u - sub);
-          atomicAdd(&s.fine[g], 1u);
-          gslot[u] = g;
+          atomicAdd(&s.fine[dbg_clamp(g, kFineMax)], 1u);
+          gslot[u] = dbg_clamp(g, kFineMax);
         }
       }
     }
-    __syncthreads();
+    row_sync();
 
     // ---- SCAN2: bucket starts ------------------------------------------------
     // fine[g] becomes start << 16 | min(size, 255) << 8, its low byte the
@@ -829,7 +837,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         incl = warp_inclusive_scan(local);
       }
       if (lane == 31) s.wa[warp] = incl;
-      __syncthreads();
+      row_sync();
       if (warp_busy) {
         const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
         const uint32_t wti = warp_inclusive_scan(wt);
@@ -857,7 +865,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         if (lane == 0 && over) s.overflow = 1u;
       }
     }
-    __syncthreads();
+    row_sync();
     fast = fast && s.overflow == 0u;
 
     float* os = out_scores + (size_t)t * (size_t)K;
@@ -876,14 +884,14 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         if (gslot[u] != kNone) {
           const uint32_t old = atomicAdd(&s.fine[gslot[u]], 1u);
           if ((old >> 16) < (uint32_t)ksel) {
-            const uint32_t pos = (old >> 16) + (old & 0xFFu);
+            const uint32_t pos = dbg_clamp((old >> 16) + (old & 0xFFu), kRankMax);
             s.live[pos] = lkey[u];
             info[pos] = (uint16_t)(old & 0xFFFFu);
             if (((old >> 8) & 0xFFu) > 1u) rkl[pos] = (lkey[u] << 11) | (255u - (old & 0xFFu));
           }
         }
       }
-      __syncthreads();
+      row_sync();
 
       // ---- RANK: position = bucket start + members ranking above ----------
       // Per list position.  Consecutive positions share buckets, so a warp's
@@ -892,8 +900,8 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       const uint32_t rbase = src.row_base(t);
       for (uint32_t p = tid; p < p_end; p += NT) {
         const uint32_t inf = info[p];
-        const uint32_t cnt = inf >> 8;
-        const uint32_t st = p - (inf & 0xFFu);
+        const uint32_t st = dbg_clamp(p - (inf & 0xFFu), p + 1u);
+        const uint32_t cnt = dbg_clamp(inf >> 8, kRankMax + 8u - st);
         const unsigned long long key = s.live[p];
         const uint32_t mc = __reduce_max_sync(__activemask(), cnt);
         uint32_t r = 0u;
@@ -928,10 +936,21 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     // SCATTER wrote the aux region through ordinary stores; the next row's
     // ids are copied into it after the barrier.
     if constexpr (Source::kStagesIds) fence_proxy_async_shared();
-    __syncthreads();  // every reader of this row's shared state is done
+    row_sync();  // every reader of this row's shared state is done
     if constexpr (Source::kStagesIds)
       if (tid == 0 && t + G < T) src.issue_ids(t + G, aux, &s.ids_bar);
 
+    if constexpr (kPoisonBuild) {
+      dbg_poison<NT>(s.fine, kFineMax + kL1Bins);
+      dbg_poison<NT>(s.live, 2 * kLiveMax);
+      dbg_poison<NT>(s.wa, 2 * kMaxWarps);
+      if constexpr (!Source::kStagesIds) dbg_poison<NT>(aux, Caps::kScratchWords);
+      if (tid == 0) {
+        s.b1 = s.nlive = s.nfine = s.above_b1 = 0xA5A5A5A5u;
+        s.found_digit = s.found_above = s.found_count = 0xA5A5A5A5u;
+      }
+      __syncthreads();
+    }
     zero_words<NT>(s.fine, kFineMax + kL1Bins);  // fine and the table behind it
     if (tid == 0) {
       s.live_cursor = 0u;

@@ -125,7 +125,7 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
       s.live_cursor = 0u;
       s.pad_n = 0u;
     }
-    __syncthreads();
+    row_sync();
     uint32_t npad = 0u;
 #pragma unroll 1
     for (int c0 = 0; c0 < n4; c0 += NT) {
@@ -161,13 +161,13 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
     }
     npad = __reduce_add_sync(0xFFFFFFFFu, npad);
     if (lane == 0 && npad != 0u) atomicAdd(&s.pad_n, npad);
-    __syncthreads();
+    row_sync();
     const uint32_t nreal = s.live_cursor;  // candidates above the padding key
     if (nreal < (uint32_t)ksel && nreal + s.pad_n >= (uint32_t)ksel) {
       int n_pow2 = 1;
       while (n_pow2 < (int)nreal) n_pow2 <<= 1;
       for (int j = (int)nreal + tid; j < n_pow2; j += NT) s.live[j] = 0ull;
-      __syncthreads();
+      row_sync();
       bitonic_sort_desc<NT>(s.live, n_pow2);
       nwin = tail = (int)nreal;
       sorted = true;
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
 #pragma unroll
     for (int v = 0; v < kVec; ++v)
       w[v] = (tid + v * NT) < n4 ? ldg4(score_chunk(v)) : make_uint4(0u, 0u, 0u, 0u);
-    __syncthreads();  // the previous row's shared state is reset
+    row_sync();  // the previous row's shared state is reset
 
     // ---- L1: histogram of the score keys' top 12 bits ----------------------
     // Also ORs the raw scores' bits below the bin: the bits that are zero in
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
     }
     raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & kLowMask);
     if (lane == 0 && raw_or) atomicOr(&s.stat_or[0], raw_or);
-    __syncthreads();
+    row_sync();
 
     // ---- SCAN1a: candidates per window of 128 bins (warp w: windows 4w..4w+3)
 #pragma unroll
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       if (lane == 0) s.wb[win] = sum;
     }
     if (tid == 0) s.pad_cnt = table[kRowsPadBin];
-    __syncthreads();
+    row_sync();
     // ---- SCAN1b: every warp scans the window totals, high to low, then ranks
     // the bins of its own windows at or above the window holding the K-th
     // key: table[b] = above(b) | count(b) << 11 | log2ceil(count(b)) << 25.
@@ -338,7 +338,8 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         }
       }
     }
-    __syncthreads();
+    row_sync();
+    dbg_poison<NT>(s.wb, kMaxWarps);  // the window totals are dead
 
     // Live candidates are those with (key >> kRefShift) >= live_from: every
     // candidate of bins >= b1, unless that overflows the live list; then the
@@ -352,20 +353,25 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         if ((tid + (j >> 2) * NT) < n4 && (keys[j] >> kL1Shift) == b1)
           atomicAdd(&s.fine[(keys[j] >> kRefShift) & 0x7FFu], 1u);
       }
-      __syncthreads();
+      row_sync();
       find_digit_desc<NT>(s.fine, (uint32_t)ksel - s.above_b1, s.wa, s.wb, s.found_digit,
                           s.found_above, s.found_count);
-      __syncthreads();
+      row_sync();
       live_from |= s.found_digit;
       const uint32_t hb = s.found_above + s.found_count;  // live candidates of bin b1
+      if constexpr (kPoisonBuild) {
+        row_sync();
+        dbg_poison<NT>(s.fine, kHistBins);
+        __syncthreads();
+      }
       zero_words<NT>(s.fine, kHistBins);
-      __syncthreads();
+      row_sync();
       if (tid == 0) {
         s.nlive = s.above_b1 + hb;
         const uint32_t q = hb > 1u ? 32u - __clz(hb - 1u) : 0u;
         table[b1] = s.above_b1 | (hb << 11) | (q << 25);
       }
-      __syncthreads();
+      row_sync();
     }
     const int nlive = (int)s.nlive;
     bool fast = nlive <= kRowsLive;
@@ -387,7 +393,8 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       const uint32_t incl = warp_inclusive_scan(cnt);
       uint32_t base = 0u;
       if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
-      unsigned long long* dst = s.live + (__shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt);
+      unsigned long long* dst =
+          s.live + dbg_clamp(__shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt, kRowsLive + 1u - cnt);
       // OR / AND of the row's inverted ids (padding's ~id of 0 left out: it
       // is the smallest, so ordering on the varying bits alone still puts
       // it last)
@@ -416,7 +423,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         atomicAnd(&s.stat_and[1], iand);
       }
     }
-    __syncthreads();
+    row_sync();
 
     // ---- L2: the position-space bucket of every live candidate -------------
     // For finite scores the key bits below the L1 bin and below tzf are equal
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
           const int d = wf - q;
           const uint32_t sub = d >= 0 ? (y >> d) : (y << (-d));
           const uint32_t cb = (tb >> 11) & 0x3FFFu;
-          const uint32_t g = (tb & 0x7FFu) + cb - 1u - ((sub * cb) >> q);
+          const uint32_t g = dbg_clamp((tb & 0x7FFu) + cb - 1u - ((sub * cb) >> q), kRowsFine);
           atomicAdd(&s.fine[g], 1u);
           gsl[u] = g;
         }
@@ -477,13 +484,14 @@ __global__ void __launch_bounds__(kRowsNT, 4)
           }
           const uint32_t sub = wy >= q ? (uint32_t)(y >> (wy - q)) : (uint32_t)(y << (q - wy));
           const uint32_t cb = (tb >> 11) & 0x3FFFu;
-          const uint32_t g = (tb & 0x7FFu) + cb - 1u - ((sub * cb) >> q);
+          const uint32_t g = dbg_clamp((tb & 0x7FFu) + cb - 1u - ((sub * cb) >> q), kRowsFine);
           atomicAdd(&s.fine[g], 1u);
           gsl[u] = g;
         }
       }
     }
-    __syncthreads();
+    row_sync();
+    dbg_poison<NT>(s.region, kRowsRegionWords);  // the bin table is dead
 
     // ---- SCAN2: bucket starts over positions [0, nlive) ---------------------
     // fine[g] becomes start << 16 | min(size, 255) << 8, its low byte the
@@ -503,7 +511,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         incl = warp_inclusive_scan(local);
       }
       if (lane == 31) s.wa[warp] = incl;
-      __syncthreads();
+      row_sync();
       if (warp_busy) {
         const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
         const uint32_t wti = warp_inclusive_scan(wt);
@@ -532,7 +540,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         if (lane == 0 && over) s.overflow = 1u;
       }
     }
-    __syncthreads();
+    row_sync();
     fast = fast && s.overflow == 0u;
 
     // the next row into L2 now: it lands during SCATTER and RANK and stays
@@ -549,7 +557,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         if (gsl[u] != kNone) {
           const uint32_t old = atomicAdd(&s.fine[gsl[u]], 1u);
           if ((old >> 16) < (uint32_t)ksel) {
-            const uint32_t pos = (old >> 16) + (old & 0xFFu);
+            const uint32_t pos = dbg_clamp((old >> 16) + (old & 0xFFu), kRowsRankMax);
             const uint32_t e = (uint32_t)(tid + u * NT);
             info[pos] = (uint16_t)(old & 0xFFFFu);
             pidx[pos] = (uint16_t)e;
@@ -560,13 +568,13 @@ __global__ void __launch_bounds__(kRowsNT, 4)
           }
         }
       }
-      __syncthreads();
+      row_sync();
       // ---- RANK: position = bucket start + members ranking above ---------
       const uint32_t p_end = min(s.p_end, (uint32_t)kRowsRankMax);
       for (uint32_t p = tid; p < p_end; p += NT) {
         const uint32_t inf = info[p];
-        const uint32_t cnt = inf >> 8;
-        const uint32_t st = p - (inf & 0xFFu);
+        const uint32_t st = dbg_clamp(p - (inf & 0xFFu), p + 1u);
+        const uint32_t cnt = dbg_clamp(inf >> 8, kRowsRankMax + 9u - st);
         const uint32_t mine = rk32[p];
         const uint32_t mc = __reduce_max_sync(__activemask(), cnt);
         uint32_t r = 0u;
@@ -584,7 +592,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         }
         const uint32_t fin = st + r;
         if (fin < (uint32_t)ksel) {
-          const unsigned long long key = s.live[pidx[p]];
+          const unsigned long long key = s.live[dbg_clamp(pidx[p], kRowsLive)];
           os[fin] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
           oi[fin] = src.out_id_from(rbase, (uint32_t)key);
         }
@@ -597,20 +605,20 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         if (gsl[u] != kNone) {
           const uint32_t old = atomicAdd(&s.fine[gsl[u]], 1u);
           if ((old >> 16) < (uint32_t)ksel) {
-            const uint32_t pos = (old >> 16) + (old & 0xFFu);
+            const uint32_t pos = dbg_clamp((old >> 16) + (old & 0xFFu), kRowsRankMax);
             const uint32_t e = (uint32_t)(tid + u * NT);
             info[pos] = (uint16_t)(old & 0xFFFFu);
             rk64[pos] = (s.live[e] << 12) | e;
           }
         }
       }
-      __syncthreads();
+      row_sync();
       // ---- RANK ----------------------------------------------------------
       const uint32_t p_end = min(s.p_end, (uint32_t)kRowsRankMax);
       for (uint32_t p = tid; p < p_end; p += NT) {
         const uint32_t inf = info[p];
-        const uint32_t cnt = inf >> 8;
-        const uint32_t st = p - (inf & 0xFFu);
+        const uint32_t st = dbg_clamp(p - (inf & 0xFFu), p + 1u);
+        const uint32_t cnt = dbg_clamp(inf >> 8, kRowsRankMax + 9u - st);
         const unsigned long long mine = rk64[p];
         const uint32_t mc = __reduce_max_sync(__activemask(), cnt);
         uint32_t r = 0u;
@@ -628,7 +636,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         }
         const uint32_t fin = st + r;
         if (fin < (uint32_t)ksel) {
-          const unsigned long long key = s.live[(uint32_t)mine & 0xFFFu];
+          const unsigned long long key = s.live[dbg_clamp((uint32_t)mine & 0xFFFu, kRowsLive)];
           os[fin] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
           oi[fin] = src.out_id_from(rbase, (uint32_t)key);
         }
@@ -636,7 +644,19 @@ __global__ void __launch_bounds__(kRowsNT, 4)
     } else {
       rows_fallback(src, s, t, n, os, oi);
     }
-    __syncthreads();  // every reader of this row's shared state is done
+    row_sync();  // every reader of this row's shared state is done
+    if constexpr (kPoisonBuild) {
+      dbg_poison<NT>(s.fine, kRowsFine + kRowsRegionWords);
+      dbg_poison<NT>(s.live, 2 * kRowsLive);
+      dbg_poison<NT>(s.wa, 2 * kMaxWarps);
+      if (tid == 0) {
+        s.b1 = s.nlive = s.above_b1 = s.pad_cnt = s.pad_n = 0xA5A5A5A5u;
+        s.found_digit = s.found_above = s.found_count = 0xA5A5A5A5u;
+        s.live_cursor = s.p_end = s.overflow = 0xA5A5A5A5u;
+        s.stat_or[0] = s.stat_or[1] = s.stat_and[0] = s.stat_and[1] = 0xA5A5A5A5u;
+      }
+      __syncthreads();
+    }
     zero_words<NT>(s.fine, kRowsFine + kRowsBins);  // fine and the histogram behind it
     if (tid == 0) {
       s.live_cursor = 0u;
