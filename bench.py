@@ -492,6 +492,32 @@ def decode_and_sweep(torch, dk, dev, stream):
         dk.library().dcp_topk_merge(*args4)
 
     out["merge_T16_dcp4_K4096_us_per_launch"] = median_of_reps(torch, raw4, stream)
+    # rows whose K-th key is -inf: merges of short shards (80% of the slots
+    # padding) and of the local top-Ks of causally masked rows
+    short = {}
+    for T in (16, 1024):
+        m = workloads.random_merge(60 + T, T, 4, 2048, mode="bf16", pad_frac=0.8)
+        s_ = torch.from_numpy(m.scores).to(dev)
+        i_ = torch.from_numpy(m.ids).to(dev)
+        oi_ = torch.empty((m.T, m.K), dtype=torch.int32, device=dev)
+        os2 = torch.empty((m.T, m.K), dtype=torch.float32, device=dev)
+        a_ = (s_.data_ptr(), i_.data_ptr(), m.T, m.dcp, m.K, None, oi_.data_ptr(), os2.data_ptr(),
+              None, 0, stream.cuda_stream)
+        short[f"padding80_T{T}_us_per_launch"] = median_of_reps(
+            torch, lambda: dk.library().dcp_topk_merge(*a_), stream, launches=50)
+    for T in (16, 1024):
+        lg = torch.from_numpy(workloads.masked_logits(T)).to(dev)
+        cs = torch.empty((4, T, 2048), dtype=torch.float32, device=dev)
+        ci = torch.empty((4, T, 2048), dtype=torch.int32, device=dev)
+        for r in range(4):
+            dk.local_topk(lg[r], 2048, r, 4, out_scores=cs[r], out_ids=ci[r], stream=stream)
+        oi_ = torch.empty((T, 2048), dtype=torch.int32, device=dev)
+        os2 = torch.empty((T, 2048), dtype=torch.float32, device=dev)
+        a_ = (cs.data_ptr(), ci.data_ptr(), T, 4, 2048, None, oi_.data_ptr(), os2.data_ptr(),
+              None, 0, stream.cuda_stream)
+        short[f"masked_merge_T{T}_us_per_launch"] = median_of_reps(
+            torch, lambda: dk.library().dcp_topk_merge(*a_), stream, launches=50)
+    out["neginf_threshold_merges"] = short
     sweep = {}
     K = 2048
     for T in workloads.SWEEP_T:

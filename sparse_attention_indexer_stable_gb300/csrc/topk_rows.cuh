@@ -103,13 +103,210 @@ __device__ __forceinline__ uint4 ldg4(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-// The fallback for one row: the row again from global memory, radix select +
-// sort (topk_core.cuh).  A row whose K-th key is padding and that has fewer
-// candidates above the padding key than K (shards shorter than K, padded
-// with (-inf, -1): one bucket of identical keys, too large for the fast
-// path) takes a shorter way: just those candidates are sorted and the tail
-// padded.  Out of line: rare, and its code stays out of the row loop.  Every
-// thread of the CTA calls it.
+// Sorts the top w of the m keys s.live[0, m) (score_key << 32 | ~id, no
+// padding among them; w <= m <= kRowsLive) and writes them, in order, to
+// positions off .. off + w - 1 of the row's output.  The same bucket
+// machinery as the row loop, on a list: a histogram of the keys' top 12
+// bits locates the bin of the w-th key; position-space buckets over the
+// bins at or above it, the bucket named by the top bits of
+// y = (key bits below the bin >> tzf) << ibf | (~id low ibf bits) with tzf
+// and ibf taken from the list itself (a list of -inf keys, whose score bits
+// are all equal, is ordered by its ids alone); a bucket rank.  Every thread
+// of the CTA calls it; it leaves s.live intact and the histogram and bucket
+// arrays dirty.  Returns false, having written nothing, if a bucket to rank
+// holds more than 255 keys (keys clustered below the bin's bits).
+template <class Source>
+__device__ bool rows_sort_list(const Source& src, RowsShared& s, int m, int w, int off,
+                               uint32_t rbase, float* os, int32_t* oi) {
+  constexpr int NT = kRowsNT;
+  constexpr int kWarpsT = NT / 32;
+  constexpr int kLivePer = kRowsLive / NT;
+  constexpr int kFinePer = kRowsFine / NT;
+  constexpr int kWindows = kRowsBins / 128;
+  constexpr int kL1Shift = kRowsL1Shift;
+  constexpr uint32_t kLowMask = (1u << kL1Shift) - 1u;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* table = s.region;
+  unsigned long long* rk64 = reinterpret_cast<unsigned long long*>(s.region);
+  uint16_t* info = reinterpret_cast<uint16_t*>(s.region + kRowsRankWords);
+  if (w <= 0 || m < w) return w <= 0;  // nothing to place (uniform)
+
+  zero_words<NT>(s.fine, kRowsFine + kRowsBins);
+  if (tid == 0) {
+    s.p_end = 0u;
+    s.overflow = 0u;
+    s.stat_or[0] = s.stat_or[1] = 0u;
+    s.stat_and[1] = 0xFFFFFFFFu;
+  }
+  row_sync();
+  // L1 over the list, with the raw scores' low bits and the ids' bits
+  {
+    uint32_t raw_or = 0u, ior = 0u, iand = 0xFFFFFFFFu;
+    for (int e = tid; e < m; e += NT) {
+      const unsigned long long lk = s.live[e];
+      const uint32_t kk = (uint32_t)(lk >> 32);
+      atomicAdd(&table[kk >> kL1Shift], 1u);
+      raw_or |= score_bits(kk);
+      ior |= (uint32_t)lk;
+      iand &= (uint32_t)lk;
+    }
+    raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & kLowMask);
+    ior = __reduce_or_sync(0xFFFFFFFFu, ior);
+    iand = __reduce_and_sync(0xFFFFFFFFu, iand);
+    if (lane == 0) {
+      atomicOr(&s.stat_or[0], raw_or);
+      atomicOr(&s.stat_or[1], ior);
+      atomicAnd(&s.stat_and[1], iand);
+    }
+  }
+  row_sync();
+  // SCAN1 as in the row loop, for the w-th key
+#pragma unroll
+  for (int j = 0; j < kWindows / kWarpsT; ++j) {
+    const int win = warp * (kWindows / kWarpsT) + j;
+    const uint4 h4 = *reinterpret_cast<const uint4*>(table + 128 * win + 4 * lane);
+    const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, h4.x + h4.y + h4.z + h4.w);
+    if (lane == 0) s.wb[win] = sum;
+  }
+  row_sync();
+  {
+    const uint32_t wt = s.wb[kWindows - 1 - lane];
+    const uint32_t wincl = warp_inclusive_scan(wt);
+#pragma unroll
+    for (int j = 0; j < kWindows / kWarpsT; ++j) {
+      const int win = warp * (kWindows / kWarpsT) + j;
+      const uint32_t above_w = __shfl_sync(0xFFFFFFFFu, wincl - wt, kWindows - 1 - win);
+      const uint32_t tot_w = __shfl_sync(0xFFFFFFFFu, wt, kWindows - 1 - win);
+      if (tot_w == 0u || above_w >= (uint32_t)w) continue;
+      const int hi = 128 * win + 127;
+      uint32_t h[4];
+      load_bins_desc<4>(table + (hi - 4 * lane - 3), h);
+      const uint32_t local = h[0] + h[1] + h[2] + h[3];
+      const uint32_t incl = warp_inclusive_scan(local);
+      uint32_t a = above_w + incl - local;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (h[e] != 0u && a < (uint32_t)w) {
+          const int b = hi - 4 * lane - e;
+          if ((uint32_t)w <= a + h[e]) {
+            s.b1 = (uint32_t)b;
+            s.nlive = a + h[e];
+          }
+          const uint32_t q = h[e] > 1u ? 32u - __clz(h[e] - 1u) : 0u;
+          table[b] = a | (h[e] << 11) | (q << 25);
+        }
+        a += h[e];
+      }
+    }
+  }
+  row_sync();
+  const uint32_t b1 = s.b1;
+  const uint32_t nsel = s.nlive;  // keys in bins >= b1: they take the buckets
+  const uint32_t ro = s.stat_or[0];
+  const uint32_t vi = s.stat_or[1] ^ s.stat_and[1];
+  const int tzf = ro ? min(__ffs(ro) - 1, kL1Shift) : kL1Shift;
+  const int ibf = vi ? 32 - __clz(vi) : 0;
+  const uint32_t imask = ibf >= 32 ? 0xFFFFFFFFu : ((1u << ibf) - 1u);
+  const int wf = kL1Shift - tzf + ibf;
+  uint32_t gsl[kLivePer];
+#pragma unroll
+  for (int u = 0; u < kLivePer; ++u) {
+    const int e = tid + u * NT;
+    gsl[u] = kNone;
+    if (e < m) {
+      const unsigned long long lk = s.live[e];
+      const uint32_t kk = (uint32_t)(lk >> 32);
+      if ((kk >> kL1Shift) >= b1) {
+        const uint32_t tb = table[kk >> kL1Shift];
+        const int q = (int)(tb >> 25);
+        const unsigned long long y =
+            ((unsigned long long)((kk & kLowMask) >> tzf) << ibf) | ((uint32_t)lk & imask);
+        const uint32_t sub = wf >= q ? (uint32_t)(y >> (wf - q)) : (uint32_t)(y << (q - wf));
+        const uint32_t cb = (tb >> 11) & 0x3FFFu;
+        const uint32_t g = dbg_clamp((tb & 0x7FFu) + cb - 1u - ((sub * cb) >> q), kRowsFine);
+        atomicAdd(&s.fine[g], 1u);
+        gsl[u] = g;
+      }
+    }
+  }
+  row_sync();
+  // SCAN2 over buckets [0, nsel)
+  {
+    const bool warp_busy = kFinePer * 32 * warp < (int)nsel;
+    uint32_t local = 0u, incl = 0u;
+    uint32_t* my = s.fine + kFinePer * tid;
+    if (warp_busy) {
+#pragma unroll
+      for (int e = 0; e < kFinePer; ++e) local += my[e];
+      incl = warp_inclusive_scan(local);
+    }
+    if (lane == 31) s.wa[warp] = incl;
+    row_sync();
+    if (warp_busy) {
+      const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
+      const uint32_t wti = warp_inclusive_scan(wt);
+      uint32_t st = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
+      uint32_t over = 0u;
+#pragma unroll
+      for (int e = 0; e < kFinePer; ++e) {
+        const uint32_t c = my[e];
+        my[e] = (st << 16) | (min(c, 255u) << 8);
+        if (st < (uint32_t)w) {
+          if (c > kBigBucket) over = 1u;
+          if ((uint32_t)w <= st + c) s.p_end = st + c;
+        }
+        st += c;
+      }
+      over = __reduce_or_sync(0xFFFFFFFFu, over);
+      if (lane == 0 && over) s.overflow = 1u;
+    }
+  }
+  row_sync();
+  if (s.overflow != 0u) return false;
+  // SCATTER and RANK
+#pragma unroll
+  for (int u = 0; u < kLivePer; ++u) {
+    if (gsl[u] != kNone) {
+      const uint32_t old = atomicAdd(&s.fine[gsl[u]], 1u);
+      if ((old >> 16) < (uint32_t)w) {
+        const uint32_t pos = dbg_clamp((old >> 16) + (old & 0xFFu), kRowsRankMax);
+        const uint32_t e = (uint32_t)(tid + u * NT);
+        info[pos] = (uint16_t)(old & 0xFFFFu);
+        rk64[pos] = (s.live[e] << 12) | e;
+      }
+    }
+  }
+  row_sync();
+  const uint32_t p_end = min(s.p_end, (uint32_t)kRowsRankMax);
+  for (uint32_t p = tid; p < p_end; p += NT) {
+    const uint32_t inf = info[p];
+    const uint32_t st = dbg_clamp(p - (inf & 0xFFu), p + 1u);
+    const uint32_t cnt = dbg_clamp(inf >> 8, kRowsRankMax + 9u - st);
+    const unsigned long long mine = rk64[p];
+    uint32_t r = 0u;
+    for (uint32_t e = 0; e < cnt; ++e) r += rk64[st + e] > mine ? 1u : 0u;
+    const uint32_t fin = st + r;
+    if (fin < (uint32_t)w) {
+      const unsigned long long key = s.live[dbg_clamp((uint32_t)mine & 0xFFFu, kRowsLive)];
+      os[off + fin] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
+      oi[off + fin] = src.out_id_from(rbase, (uint32_t)key);
+    }
+  }
+  row_sync();
+  return true;
+}
+
+// The fallback for one row, the row read again from global memory.
+// - A row whose K-th key is -inf (fewer finite candidates than K: shards
+//   shorter than K padded with (-inf, -1), or masked rows whose local top-K
+//   holds real -inf candidates): the finite candidates are all winners and
+//   are sorted as a list; the next winners are the real -inf candidates with
+//   the lowest ids (a radix select on the id first when there are more of
+//   them than the list holds), sorted as a list; padding fills the rest.
+// - Otherwise (buckets too large, or negative NaNs among the winners): the
+//   radix select + sort of topk_core.cuh over the whole row.
+// Out of line: rare, and its code stays out of the row loop.  Every thread
+// of the CTA calls it.
 template <class Source>
 __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int t, int n,
                                            float* os, int32_t* oi) {
@@ -117,16 +314,17 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
   constexpr int ksel = kRowsK;
   const int tid = threadIdx.x, lane = tid & 31;
   const int n4 = n >> 2;
-  int nwin = ksel, tail = ksel;  // winners in s.live[0, nwin), sorted; padding from tail on
-  bool sorted = false;
+  const uint32_t rbase = src.row_base(t);
   SelectShared& sel = *reinterpret_cast<SelectShared*>(s.region);
   if (s.b1 == kRowsPadBin) {
+    // finite candidates into the list; real -inf and padding counted
     if (tid == 0) {
       s.live_cursor = 0u;
       s.pad_n = 0u;
+      s.found_count = 0u;  // here: the real -inf candidates
     }
     row_sync();
-    uint32_t npad = 0u;
+    uint32_t npad = 0u, nreal_inf = 0u;
 #pragma unroll 1
     for (int c0 = 0; c0 < n4; c0 += NT) {
       const int c = c0 + tid;
@@ -138,56 +336,115 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
       }
       const uint32_t ks[4] = {k4.x, k4.y, k4.z, k4.w};
       const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
-      uint32_t m = 0u;
+      uint32_t fm = 0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         if (c < n4) {
-          if (ks[e] > kNegInfKey || (ks[e] == kNegInfKey && us[e] != 0u)) m |= 1u << e;
+          fm |= (ks[e] > kNegInfKey ? 1u : 0u) << e;
           npad += (ks[e] == kNegInfKey && us[e] == 0u) ? 1u : 0u;
+          nreal_inf += (ks[e] == kNegInfKey && us[e] != 0u) ? 1u : 0u;
         }
       }
-      const uint32_t cnt = __popc(m);
+      const uint32_t cnt = __popc(fm);
       const uint32_t incl = warp_inclusive_scan(cnt);
       uint32_t base = 0u;
       if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
       uint32_t slot = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (m & (1u << e)) {
+        if (fm & (1u << e)) {
           if (slot < (uint32_t)kRowsLive) s.live[slot] = ((unsigned long long)ks[e] << 32) | us[e];
           ++slot;
         }
       }
     }
     npad = __reduce_add_sync(0xFFFFFFFFu, npad);
-    if (lane == 0 && npad != 0u) atomicAdd(&s.pad_n, npad);
+    nreal_inf = __reduce_add_sync(0xFFFFFFFFu, nreal_inf);
+    if (lane == 0) {
+      if (npad != 0u) atomicAdd(&s.pad_n, npad);
+      if (nreal_inf != 0u) atomicAdd(&s.found_count, nreal_inf);
+    }
     row_sync();
-    const uint32_t nreal = s.live_cursor;  // candidates above the padding key
-    if (nreal < (uint32_t)ksel && nreal + s.pad_n >= (uint32_t)ksel) {
-      int n_pow2 = 1;
-      while (n_pow2 < (int)nreal) n_pow2 <<= 1;
-      for (int j = (int)nreal + tid; j < n_pow2; j += NT) s.live[j] = 0ull;
-      row_sync();
-      bitonic_sort_desc<NT>(s.live, n_pow2);
-      nwin = tail = (int)nreal;
-      sorted = true;
+    const uint32_t nfin = s.live_cursor;     // finite candidates (above -inf)
+    const uint32_t rinf = s.found_count;     // real -inf candidates
+    const uint32_t npd = s.pad_n;            // padding
+    if (nfin < (uint32_t)ksel && nfin + rinf + npd >= (uint32_t)ksel) {
+      bool ok = nfin == 0u || rows_sort_list(src, s, (int)nfin, (int)nfin, 0, rbase, os, oi);
+      const uint32_t w2 = min(rinf, (uint32_t)ksel - nfin);  // -inf winners
+      if (ok && w2 > 0u) {
+        // the real -inf candidates with the lowest ids: the list holds them
+        // all, or a radix select on ~id finds the w2 largest first
+        RadixResult rr{0u, 0u, 0u, 0u};
+        const bool select = rinf > (uint32_t)kRowsLive;
+        if (select)
+          rr = radix_select<NT>(sel, n, w2, [&](int i, uint32_t& v) {
+            v = src.inv_global(t, i);
+            return v != 0u && src.key_global(t, i) == kNegInfKey;
+          });
+        if (tid == 0) {
+          s.live_cursor = 0u;
+          sel.dup_claim = 0u;
+        }
+        row_sync();
+#pragma unroll 1
+        for (int c0 = 0; c0 < n4; c0 += NT) {
+          const int c = c0 + tid;
+          uint32_t fm = 0u;
+          uint4 u4 = make_uint4(0u, 0u, 0u, 0u);
+          if (c < n4) {
+            const uint4 k4 = src.key4_global(t, c);
+            const uint4 i4 = src.ids4_global(t, c);
+            u4 = make_uint4(~i4.x, ~i4.y, ~i4.z, ~i4.w);
+            const uint32_t ks[4] = {k4.x, k4.y, k4.z, k4.w};
+            const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              bool in = ks[e] == kNegInfKey && us[e] != 0u;
+              if (in && select) {
+                const uint32_t um = us[e] & rr.mask;
+                // identical ids at the threshold (outside the contract): the
+                // first ones claimed fill the slots left
+                in = um > rr.prefix ||
+                     (um == rr.prefix && (rr.need == rr.count || atomicAdd(&sel.dup_claim, 1u) < rr.need));
+              }
+              fm |= (in ? 1u : 0u) << e;
+            }
+          }
+          const uint32_t cnt = __popc(fm);
+          const uint32_t incl = warp_inclusive_scan(cnt);
+          uint32_t base = 0u;
+          if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
+          uint32_t slot = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+          const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (fm & (1u << e)) {
+              if (slot < (uint32_t)kRowsLive)
+                s.live[slot] = ((unsigned long long)kNegInfKey << 32) | us[e];
+              ++slot;
+            }
+          }
+        }
+        row_sync();
+        const uint32_t m2 = min(s.live_cursor, (uint32_t)kRowsLive);
+        ok = rows_sort_list(src, s, (int)m2, (int)min(w2, m2), (int)nfin, rbase, os, oi);
+      }
+      if (ok) {
+        for (int j = (int)(nfin + w2) + tid; j < ksel; j += NT) {
+          os[j] = __uint_as_float(0xFF800000u);  // -inf
+          oi[j] = -1;
+        }
+        return;
+      }
     }
   }
-  if (!sorted) {
-    select_sort_row<NT>(
-        sel, n, ksel, s.live, ksel, [&](int i) { return src.key_global(t, i); },
-        [&](int i) { return src.inv_global(t, i); });
-  }
-  const uint32_t rbase = src.row_base(t);
+  select_sort_row<NT>(
+      sel, n, ksel, s.live, ksel, [&](int i) { return src.key_global(t, i); },
+      [&](int i) { return src.inv_global(t, i); });
   for (int j = tid; j < ksel; j += NT) {
-    if (j < nwin) {
-      const unsigned long long w = s.live[j];
-      os[j] = __uint_as_float(score_bits((uint32_t)(w >> 32)));
-      oi[j] = src.out_id_from(rbase, (uint32_t)w);
-    } else if (j >= tail) {
-      os[j] = __uint_as_float(0xFF800000u);  // -inf
-      oi[j] = -1;
-    }
+    const unsigned long long w = s.live[j];
+    os[j] = __uint_as_float(score_bits((uint32_t)(w >> 32)));
+    oi[j] = src.out_id_from(rbase, (uint32_t)w);
   }
 }
 

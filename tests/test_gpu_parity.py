@@ -551,3 +551,24 @@ def test_graph_captured_prefill_chunks():
     g2.replay()
     torch.cuda.synchronize()
     assert_same((out_ids.cpu().numpy()[rows], out_scores.cpu().numpy()[rows]), want, "per chunk")
+
+
+@pytest.mark.parametrize("T", [16, 300])
+def test_masked_sweep_merge(T):
+    """The merge of the local top-Ks of causally masked rows (rows of
+    differing context length): shards seeing fewer than K tokens contribute
+    real -inf candidates, and rows seeing fewer than K tokens in all have a
+    K-th key of -inf.  The merge must equal the oracle's merge of the same
+    candidates, and (composition) the fused top-K of the logits."""
+    x = workloads.masked_logits(T, seed=6 + T)
+    dcp, _, L = x.shape
+    K = 2048
+    cs = np.empty((dcp, T, K), np.float32)
+    ci = np.empty((dcp, T, K), np.int32)
+    for r in range(dcp):
+        cs[r], ci[r] = oracle.local_topk(x[r], K, r, dcp)
+    m = workloads.Merge("masked", cs, ci)
+    got = run_merge(m)
+    assert_same(got, oracle.merge(cs, ci), "masked merge")
+    fs, fi = oracle.fused_topk(x, K)
+    assert_same(got, (fi, fs), "masked merge vs fused")

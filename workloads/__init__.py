@@ -206,6 +206,25 @@ def random_merge(seed: int, T: int, dcp: int, K: int, mode: str = "normal",
     return Merge(f"random-{mode}", scores, ids, rs)
 
 
+def masked_logits(T: int, seed: int = 5, dcp: int = 4, L: int = 4096) -> np.ndarray:
+    """Per-shard logits (dcp, T, L) of prefill rows with differing context
+    lengths: row t sees the first c_t tokens of the sequence (c_t uniform in
+    [1, dcp*L], seeded), the tokens dealt to the shards contiguously (shard r
+    holds tokens [r*L, (r+1)*L)), so shard r's row t has max(0, min(L,
+    c_t - r*L)) finite logits (N(0,1) rounded to bf16) and -inf after them
+    (the causal mask).  The local top-K of each shard then holds real -inf
+    candidates wherever a shard sees fewer than K tokens, and the merge of
+    those rows has a K-th key of -inf whenever the row sees fewer than K
+    tokens in all."""
+    rng = np.random.default_rng(seed)
+    x = round_to_bf16(rng.standard_normal((dcp, T, L), dtype=np.float32))
+    ctx = rng.integers(1, dcp * L + 1, T)
+    for r in range(dcp):
+        valid = np.clip(ctx - r * L, 0, L)
+        x[r][np.arange(L)[None, :] >= valid[:, None]] = NEG_INF
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
 def random_logits(seed: int, T: int, L: int, ld: int | None = None, mode: str = "bf16") -> np.ndarray:
     """Logits rows (T, ld) with the first L columns meaningful.
 
