@@ -116,6 +116,7 @@ struct StreamShared {
   uint32_t p_end;                     // end of the bucket straddling K
   uint32_t overflow;                  // a bucket to rank is too large
   uint32_t pad_n;                     // fallback: padding keys of the row
+  uint32_t lscal[8];                  // list_sort's scalars
   unsigned long long stage_bar;       // completes when a row's scores land in the stage
   unsigned long long ids_bar;         // completes when a row's ids land in the aux region
 };
@@ -315,6 +316,216 @@ __device__ __forceinline__ void zero_words(uint32_t* p, int words) {
     *reinterpret_cast<uint4*>(p + i) = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// Scratch of list_sort: pointers into the calling kernel's shared memory.
+struct ListScratch {
+  const unsigned long long* list;  // the keys score_key << 32 | ~id (read only)
+  uint32_t* fine;                  // >= the list's length (bucket sizes)
+  uint32_t* table;                 // the histogram: 2^kBits words
+  unsigned long long* rk;          // >= w + 255 keys (the bucket-ordered list)
+  uint16_t* info;                  // as many entries: bucket size << 8 | slot
+  uint32_t* wa;                    // 32 words
+  uint32_t* wb;                    // 32 words
+  uint32_t* scal;                  // 8 words
+};
+
+// Sorts the top w of the m keys list[0, m) (no padding among them;
+// 0 < w <= m <= kCap) and hands them, in order, to out(position, key):
+// the bucket machinery of the row kernels applied to a list.  A histogram of
+// the keys' top kBits bits locates the bin of the w-th key; the bins at or
+// above it get buckets in position space (bin b owns buckets
+// [above(b), above(b) + count(b))), each key going to the bucket named by the
+// top bits of y = (key bits below the bin >> tzf) << ibf | (~id low ibf bits),
+// tzf and ibf taken from the list itself, so a list of -inf keys, whose
+// score bits are all equal, is ordered by its ids alone; a bucket's members
+// are ranked by comparing their keys, identical keys (outside the contract)
+// by their slots.  Every thread of the CTA calls it; returns false, having
+// output nothing, if a bucket to rank holds more than 255 keys (keys that
+// agree on every bit the buckets use).
+template <int NT, int kBits, int kCap, class Out>
+__device__ bool list_sort(const ListScratch& ls, int m, int w, Out out) {
+  constexpr int kWarpsT = NT / 32;
+  constexpr int kShift = 32 - kBits;
+  constexpr uint32_t kLowMask = (1u << kShift) - 1u;
+  constexpr int kBins = 1 << kBits;
+  constexpr int kWindows = kBins / 128;
+  constexpr int kPer = (kCap + NT - 1) / NT;
+  static_assert(kWindows <= 32, "one lane per window");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* table = ls.table;
+  uint32_t* fine = ls.fine;
+  uint32_t& b1_s = ls.scal[0];
+  uint32_t& nsel_s = ls.scal[1];
+  uint32_t& p_end_s = ls.scal[2];
+  uint32_t& over_s = ls.scal[3];
+  uint32_t& ro_s = ls.scal[4];
+  uint32_t& ior_s = ls.scal[5];
+  uint32_t& iand_s = ls.scal[6];
+  if (w <= 0 || m < w || m > kCap) return w <= 0;  // uniform
+
+  zero_words<NT>(fine, (m + 3) & ~3);
+  zero_words<NT>(table, kBins);
+  if (tid == 0) {
+    p_end_s = over_s = ro_s = ior_s = 0u;
+    iand_s = 0xFFFFFFFFu;
+  }
+  row_sync();
+  {
+    uint32_t raw_or = 0u, ior = 0u, iand = 0xFFFFFFFFu;
+    for (int e = tid; e < m; e += NT) {
+      const unsigned long long lk = ls.list[e];
+      const uint32_t kk = (uint32_t)(lk >> 32);
+      atomicAdd(&table[kk >> kShift], 1u);
+      raw_or |= score_bits(kk);
+      ior |= (uint32_t)lk;
+      iand &= (uint32_t)lk;
+    }
+    raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & kLowMask);
+    ior = __reduce_or_sync(0xFFFFFFFFu, ior);
+    iand = __reduce_and_sync(0xFFFFFFFFu, iand);
+    if (lane == 0) {
+      atomicOr(&ro_s, raw_or);
+      atomicOr(&ior_s, ior);
+      atomicAnd(&iand_s, iand);
+    }
+  }
+  row_sync();
+  // bin totals per window of 128 bins
+  for (int win = warp; win < kWindows; win += kWarpsT) {
+    const uint4 h4 = *reinterpret_cast<const uint4*>(table + 128 * win + 4 * lane);
+    const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, h4.x + h4.y + h4.z + h4.w);
+    if (lane == 0) ls.wb[win] = sum;
+  }
+  row_sync();
+  // every warp scans the window totals (high to low) and ranks the bins of
+  // its windows at or above the w-th key: above | count << 13 | q << 26
+  {
+    const uint32_t wt = lane < kWindows ? ls.wb[kWindows - 1 - lane] : 0u;
+    const uint32_t wincl = warp_inclusive_scan(wt);
+    for (int win = warp; win < kWindows; win += kWarpsT) {
+      const uint32_t above_w = __shfl_sync(0xFFFFFFFFu, wincl - wt, kWindows - 1 - win);
+      const uint32_t tot_w = __shfl_sync(0xFFFFFFFFu, wt, kWindows - 1 - win);
+      if (tot_w == 0u || above_w >= (uint32_t)w) continue;
+      const int hi = 128 * win + 127;
+      uint32_t h[4];
+      load_bins_desc<4>(table + (hi - 4 * lane - 3), h);
+      const uint32_t local = h[0] + h[1] + h[2] + h[3];
+      const uint32_t incl = warp_inclusive_scan(local);
+      uint32_t a = above_w + incl - local;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (h[e] != 0u && a < (uint32_t)w) {
+          const int b = hi - 4 * lane - e;
+          if ((uint32_t)w <= a + h[e]) {
+            b1_s = (uint32_t)b;
+            nsel_s = a + h[e];
+          }
+          const uint32_t q = h[e] > 1u ? 32u - __clz(h[e] - 1u) : 0u;
+          table[b] = a | (h[e] << 13) | (q << 26);
+        }
+        a += h[e];
+      }
+    }
+  }
+  row_sync();
+  const uint32_t b1 = b1_s;
+  const uint32_t nsel = nsel_s;  // keys in bins >= b1: they take the buckets
+  const uint32_t ro = ro_s;
+  const uint32_t vi = ior_s ^ iand_s;
+  const int tzf = ro ? min(__ffs(ro) - 1, kShift) : kShift;
+  const int ibf = vi ? 32 - __clz(vi) : 0;
+  const uint32_t imask = ibf >= 32 ? 0xFFFFFFFFu : ((1u << ibf) - 1u);
+  const int wf = kShift - tzf + ibf;
+  uint32_t gsl[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = tid + u * NT;
+    gsl[u] = kNone;
+    if (e < m) {
+      const unsigned long long lk = ls.list[e];
+      const uint32_t kk = (uint32_t)(lk >> 32);
+      if ((kk >> kShift) >= b1) {
+        const uint32_t tb = table[kk >> kShift];
+        const int q = (int)(tb >> 26);
+        const unsigned long long y =
+            ((unsigned long long)((kk & kLowMask) >> tzf) << ibf) | ((uint32_t)lk & imask);
+        const uint32_t sub = wf >= q ? (uint32_t)(y >> (wf - q)) : (uint32_t)(y << (q - wf));
+        const uint32_t cb = (tb >> 13) & 0x1FFFu;
+        const uint32_t g = dbg_clamp((tb & 0x1FFFu) + cb - 1u - ((sub * cb) >> q), nsel);
+        atomicAdd(&fine[g], 1u);
+        gsl[u] = g;
+      }
+    }
+  }
+  row_sync();
+  // bucket starts over [0, nsel)
+  {
+    uint32_t local = 0u;
+    uint32_t c[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int g = kPer * tid + u;
+      c[u] = g < (int)nsel ? fine[g] : 0u;
+      local += c[u];
+    }
+    const uint32_t incl = warp_inclusive_scan(local);
+    if (lane == 31) ls.wa[warp] = incl;
+    row_sync();
+    const uint32_t wt = lane < kWarpsT ? ls.wa[lane] : 0u;
+    const uint32_t wti = warp_inclusive_scan(wt);
+    uint32_t st = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
+    uint32_t over = 0u;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int g = kPer * tid + u;
+      if (g < (int)nsel) {
+        fine[g] = (st << 16) | (min(c[u], 255u) << 8);
+        if (st < (uint32_t)w) {
+          if (c[u] > kBigBucket) over = 1u;
+          if ((uint32_t)w <= st + c[u]) p_end_s = st + c[u];
+        }
+      }
+      st += c[u];
+    }
+    over = __reduce_or_sync(0xFFFFFFFFu, over);
+    if (lane == 0 && over) over_s = 1u;
+  }
+  row_sync();
+  if (over_s != 0u) return false;
+  // the keys of buckets starting before w into their bucket's slots
+  const uint32_t p_cap = (uint32_t)w + kBigBucket;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    if (gsl[u] != kNone) {
+      const uint32_t old = atomicAdd(&fine[gsl[u]], 1u);
+      if ((old >> 16) < (uint32_t)w) {
+        const uint32_t pos = dbg_clamp((old >> 16) + (old & 0xFFu), p_cap);
+        ls.info[pos] = (uint16_t)(old & 0xFFFFu);
+        ls.rk[pos] = ls.list[tid + u * NT];
+      }
+    }
+  }
+  row_sync();
+  // rank within the bucket: the members with larger keys, and identical
+  // keys in earlier slots
+  const uint32_t p_end = min(p_end_s, p_cap);
+  for (uint32_t p = tid; p < p_end; p += NT) {
+    const uint32_t inf = ls.info[p];
+    const uint32_t slot = inf & 0xFFu;
+    const uint32_t st = dbg_clamp(p - slot, p + 1u);
+    const uint32_t cnt = dbg_clamp(inf >> 8, p_cap + 1u - st);
+    const unsigned long long mine = ls.rk[p];
+    uint32_t r = 0u;
+    for (uint32_t e = 0; e < cnt; ++e) {
+      const unsigned long long x = ls.rk[st + e];
+      r += (x > mine || (x == mine && e < slot)) ? 1u : 0u;
+    }
+    const uint32_t fin = st + r;
+    if (fin < (uint32_t)w) out(fin, mine);
+  }
+  row_sync();
+  return true;
+}
+
 // The fallback for one row of the streaming kernel: the row again from
 // global memory, radix select + sort (topk_core.cuh).  Two kinds of rows
 // whose K-th key is -inf take a shorter way:
@@ -337,6 +548,16 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
   int nwin = ksel;  // winners in s.live[0, nwin), sorted
   int tail = ksel;  // padding from here on (positions nwin .. tail are written)
   bool sorted = false;
+  // list_sort's scratch: the table and bucket arrays, RANK's scratch in the
+  // aux region (the staged ids are read before it is written)
+  unsigned long long* lrk = reinterpret_cast<unsigned long long*>(const_cast<uint32_t*>(aux));
+  const ListScratch ls{s.live, s.fine, s.u.table, lrk,
+                       reinterpret_cast<uint16_t*>(lrk + Caps::kRankMax), s.wa, s.wb, s.lscal};
+  const uint32_t rbase0 = src.row_base(t);
+  auto out_at = [&](uint32_t pos, unsigned long long key) {
+    os[pos] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
+    oi[pos] = src.out_id_from(rbase0, (uint32_t)key);
+  };
   if constexpr (Source::kStagesIds) {
     if (s.b1 == Caps::kPadBin) {
       if (tid == 0) s.live_cursor = 0u;  // COMPACT's last use was barriers ago
@@ -377,13 +598,10 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
       if (lane == 0 && npad != 0u) atomicAdd(&s.pad_n, npad);
       row_sync();
       const uint32_t nreal = s.live_cursor;  // candidates above the padding key
-      if (nreal < (uint32_t)ksel && nreal + s.pad_n >= (uint32_t)ksel) {
-        int n_pow2 = 1;
-        while (n_pow2 < (int)nreal) n_pow2 <<= 1;
-        for (int j = (int)nreal + tid; j < n_pow2; j += NT) s.live[j] = 0ull;
-        row_sync();
-        bitonic_sort_desc<NT>(s.live, n_pow2);
-        nwin = tail = (int)nreal;
+      if (nreal < (uint32_t)ksel && nreal + s.pad_n >= (uint32_t)ksel &&
+          list_sort<NT, Caps::kL1Bits, Caps::kLive>(ls, (int)nreal, (int)nreal, out_at)) {
+        nwin = 0;  // the winners are written; padding from nreal on
+        tail = (int)nreal;
         sorted = true;
       }
     }
@@ -471,13 +689,11 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
           before += chunk;
           row_sync();  // s.wa is rewritten by the next chunk
         }
-        int n_pow2 = 1;
-        while (n_pow2 < (int)nf) n_pow2 <<= 1;
-        for (int j = (int)nf + tid; j < n_pow2; j += NT) s.live[j] = 0ull;
-        row_sync();
-        bitonic_sort_desc<NT>(s.live, n_pow2);
-        nwin = (int)nf;
-        sorted = true;
+        if (list_sort<NT, Caps::kL1Bits, Caps::kLive>(ls, (int)nf, (int)nf, out_at)) {
+          nwin = 0;  // the finite winners are written, the -inf ones above
+          tail = ksel;
+          sorted = true;
+        }
       }
     }
   }

@@ -85,6 +85,7 @@ struct RowsShared {
   uint32_t overflow;                   // a bucket to rank is too large
   uint32_t pad_cnt;                    // candidates in the -inf bin
   uint32_t pad_n;                      // fallback: padding candidates
+  uint32_t lscal[8];                   // list_sort's scalars
 };
 static_assert(offsetof(RowsShared, region) == sizeof(uint32_t) * kRowsFine,
               "fine and the histogram are one region to reset");
@@ -101,199 +102,6 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 
 __device__ __forceinline__ uint4 ldg4(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
-}
-
-// Sorts the top w of the m keys s.live[0, m) (score_key << 32 | ~id, no
-// padding among them; w <= m <= kRowsLive) and writes them, in order, to
-// positions off .. off + w - 1 of the row's output.  The same bucket
-// machinery as the row loop, on a list: a histogram of the keys' top 12
-// bits locates the bin of the w-th key; position-space buckets over the
-// bins at or above it, the bucket named by the top bits of
-// y = (key bits below the bin >> tzf) << ibf | (~id low ibf bits) with tzf
-// and ibf taken from the list itself (a list of -inf keys, whose score bits
-// are all equal, is ordered by its ids alone); a bucket rank.  Every thread
-// of the CTA calls it; it leaves s.live intact and the histogram and bucket
-// arrays dirty.  Returns false, having written nothing, if a bucket to rank
-// holds more than 255 keys (keys clustered below the bin's bits).
-template <class Source>
-__device__ bool rows_sort_list(const Source& src, RowsShared& s, int m, int w, int off,
-                               uint32_t rbase, float* os, int32_t* oi) {
-  constexpr int NT = kRowsNT;
-  constexpr int kWarpsT = NT / 32;
-  constexpr int kLivePer = kRowsLive / NT;
-  constexpr int kFinePer = kRowsFine / NT;
-  constexpr int kWindows = kRowsBins / 128;
-  constexpr int kL1Shift = kRowsL1Shift;
-  constexpr uint32_t kLowMask = (1u << kL1Shift) - 1u;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t* table = s.region;
-  unsigned long long* rk64 = reinterpret_cast<unsigned long long*>(s.region);
-  uint16_t* info = reinterpret_cast<uint16_t*>(s.region + kRowsRankWords);
-  if (w <= 0 || m < w) return w <= 0;  // nothing to place (uniform)
-
-  zero_words<NT>(s.fine, kRowsFine + kRowsBins);
-  if (tid == 0) {
-    s.p_end = 0u;
-    s.overflow = 0u;
-    s.stat_or[0] = s.stat_or[1] = 0u;
-    s.stat_and[1] = 0xFFFFFFFFu;
-  }
-  row_sync();
-  // L1 over the list, with the raw scores' low bits and the ids' bits
-  {
-    uint32_t raw_or = 0u, ior = 0u, iand = 0xFFFFFFFFu;
-    for (int e = tid; e < m; e += NT) {
-      const unsigned long long lk = s.live[e];
-      const uint32_t kk = (uint32_t)(lk >> 32);
-      atomicAdd(&table[kk >> kL1Shift], 1u);
-      raw_or |= score_bits(kk);
-      ior |= (uint32_t)lk;
-      iand &= (uint32_t)lk;
-    }
-    raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & kLowMask);
-    ior = __reduce_or_sync(0xFFFFFFFFu, ior);
-    iand = __reduce_and_sync(0xFFFFFFFFu, iand);
-    if (lane == 0) {
-      atomicOr(&s.stat_or[0], raw_or);
-      atomicOr(&s.stat_or[1], ior);
-      atomicAnd(&s.stat_and[1], iand);
-    }
-  }
-  row_sync();
-  // SCAN1 as in the row loop, for the w-th key
-#pragma unroll
-  for (int j = 0; j < kWindows / kWarpsT; ++j) {
-    const int win = warp * (kWindows / kWarpsT) + j;
-    const uint4 h4 = *reinterpret_cast<const uint4*>(table + 128 * win + 4 * lane);
-    const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, h4.x + h4.y + h4.z + h4.w);
-    if (lane == 0) s.wb[win] = sum;
-  }
-  row_sync();
-  {
-    const uint32_t wt = s.wb[kWindows - 1 - lane];
-    const uint32_t wincl = warp_inclusive_scan(wt);
-#pragma unroll
-    for (int j = 0; j < kWindows / kWarpsT; ++j) {
-      const int win = warp * (kWindows / kWarpsT) + j;
-      const uint32_t above_w = __shfl_sync(0xFFFFFFFFu, wincl - wt, kWindows - 1 - win);
-      const uint32_t tot_w = __shfl_sync(0xFFFFFFFFu, wt, kWindows - 1 - win);
-      if (tot_w == 0u || above_w >= (uint32_t)w) continue;
-      const int hi = 128 * win + 127;
-      uint32_t h[4];
-      load_bins_desc<4>(table + (hi - 4 * lane - 3), h);
-      const uint32_t local = h[0] + h[1] + h[2] + h[3];
-      const uint32_t incl = warp_inclusive_scan(local);
-      uint32_t a = above_w + incl - local;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (h[e] != 0u && a < (uint32_t)w) {
-          const int b = hi - 4 * lane - e;
-          if ((uint32_t)w <= a + h[e]) {
-            s.b1 = (uint32_t)b;
-            s.nlive = a + h[e];
-          }
-          const uint32_t q = h[e] > 1u ? 32u - __clz(h[e] - 1u) : 0u;
-          table[b] = a | (h[e] << 11) | (q << 25);
-        }
-        a += h[e];
-      }
-    }
-  }
-  row_sync();
-  const uint32_t b1 = s.b1;
-  const uint32_t nsel = s.nlive;  // keys in bins >= b1: they take the buckets
-  const uint32_t ro = s.stat_or[0];
-  const uint32_t vi = s.stat_or[1] ^ s.stat_and[1];
-  const int tzf = ro ? min(__ffs(ro) - 1, kL1Shift) : kL1Shift;
-  const int ibf = vi ? 32 - __clz(vi) : 0;
-  const uint32_t imask = ibf >= 32 ? 0xFFFFFFFFu : ((1u << ibf) - 1u);
-  const int wf = kL1Shift - tzf + ibf;
-  uint32_t gsl[kLivePer];
-#pragma unroll
-  for (int u = 0; u < kLivePer; ++u) {
-    const int e = tid + u * NT;
-    gsl[u] = kNone;
-    if (e < m) {
-      const unsigned long long lk = s.live[e];
-      const uint32_t kk = (uint32_t)(lk >> 32);
-      if ((kk >> kL1Shift) >= b1) {
-        const uint32_t tb = table[kk >> kL1Shift];
-        const int q = (int)(tb >> 25);
-        const unsigned long long y =
-            ((unsigned long long)((kk & kLowMask) >> tzf) << ibf) | ((uint32_t)lk & imask);
-        const uint32_t sub = wf >= q ? (uint32_t)(y >> (wf - q)) : (uint32_t)(y << (q - wf));
-        const uint32_t cb = (tb >> 11) & 0x3FFFu;
-        const uint32_t g = dbg_clamp((tb & 0x7FFu) + cb - 1u - ((sub * cb) >> q), kRowsFine);
-        atomicAdd(&s.fine[g], 1u);
-        gsl[u] = g;
-      }
-    }
-  }
-  row_sync();
-  // SCAN2 over buckets [0, nsel)
-  {
-    const bool warp_busy = kFinePer * 32 * warp < (int)nsel;
-    uint32_t local = 0u, incl = 0u;
-    uint32_t* my = s.fine + kFinePer * tid;
-    if (warp_busy) {
-#pragma unroll
-      for (int e = 0; e < kFinePer; ++e) local += my[e];
-      incl = warp_inclusive_scan(local);
-    }
-    if (lane == 31) s.wa[warp] = incl;
-    row_sync();
-    if (warp_busy) {
-      const uint32_t wt = lane < kWarpsT ? s.wa[lane] : 0u;
-      const uint32_t wti = warp_inclusive_scan(wt);
-      uint32_t st = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
-      uint32_t over = 0u;
-#pragma unroll
-      for (int e = 0; e < kFinePer; ++e) {
-        const uint32_t c = my[e];
-        my[e] = (st << 16) | (min(c, 255u) << 8);
-        if (st < (uint32_t)w) {
-          if (c > kBigBucket) over = 1u;
-          if ((uint32_t)w <= st + c) s.p_end = st + c;
-        }
-        st += c;
-      }
-      over = __reduce_or_sync(0xFFFFFFFFu, over);
-      if (lane == 0 && over) s.overflow = 1u;
-    }
-  }
-  row_sync();
-  if (s.overflow != 0u) return false;
-  // SCATTER and RANK
-#pragma unroll
-  for (int u = 0; u < kLivePer; ++u) {
-    if (gsl[u] != kNone) {
-      const uint32_t old = atomicAdd(&s.fine[gsl[u]], 1u);
-      if ((old >> 16) < (uint32_t)w) {
-        const uint32_t pos = dbg_clamp((old >> 16) + (old & 0xFFu), kRowsRankMax);
-        const uint32_t e = (uint32_t)(tid + u * NT);
-        info[pos] = (uint16_t)(old & 0xFFFFu);
-        rk64[pos] = (s.live[e] << 12) | e;
-      }
-    }
-  }
-  row_sync();
-  const uint32_t p_end = min(s.p_end, (uint32_t)kRowsRankMax);
-  for (uint32_t p = tid; p < p_end; p += NT) {
-    const uint32_t inf = info[p];
-    const uint32_t st = dbg_clamp(p - (inf & 0xFFu), p + 1u);
-    const uint32_t cnt = dbg_clamp(inf >> 8, kRowsRankMax + 9u - st);
-    const unsigned long long mine = rk64[p];
-    uint32_t r = 0u;
-    for (uint32_t e = 0; e < cnt; ++e) r += rk64[st + e] > mine ? 1u : 0u;
-    const uint32_t fin = st + r;
-    if (fin < (uint32_t)w) {
-      const unsigned long long key = s.live[dbg_clamp((uint32_t)mine & 0xFFFu, kRowsLive)];
-      os[off + fin] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
-      oi[off + fin] = src.out_id_from(rbase, (uint32_t)key);
-    }
-  }
-  row_sync();
-  return true;
 }
 
 // The fallback for one row, the row read again from global memory.
@@ -316,6 +124,16 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
   const int n4 = n >> 2;
   const uint32_t rbase = src.row_base(t);
   SelectShared& sel = *reinterpret_cast<SelectShared*>(s.region);
+  // list_sort's scratch: the histogram, then RANK's scratch, in the region
+  const ListScratch ls{s.live, s.fine, s.region,
+                       reinterpret_cast<unsigned long long*>(s.region),
+                       reinterpret_cast<uint16_t*>(s.region + kRowsRankWords), s.wa, s.wb,
+                       s.lscal};
+  int off = 0;
+  auto out_at = [&](uint32_t pos, unsigned long long key) {
+    os[off + (int)pos] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
+    oi[off + (int)pos] = src.out_id_from(rbase, (uint32_t)key);
+  };
   if (s.b1 == kRowsPadBin) {
     // finite candidates into the list; real -inf and padding counted
     if (tid == 0) {
@@ -369,7 +187,7 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
     const uint32_t rinf = s.found_count;     // real -inf candidates
     const uint32_t npd = s.pad_n;            // padding
     if (nfin < (uint32_t)ksel && nfin + rinf + npd >= (uint32_t)ksel) {
-      bool ok = nfin == 0u || rows_sort_list(src, s, (int)nfin, (int)nfin, 0, rbase, os, oi);
+      bool ok = list_sort<NT, 12, kRowsLive>(ls, (int)nfin, (int)nfin, out_at);
       const uint32_t w2 = min(rinf, (uint32_t)ksel - nfin);  // -inf winners
       if (ok && w2 > 0u) {
         // the real -inf candidates with the lowest ids: the list holds them
@@ -427,7 +245,8 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
         }
         row_sync();
         const uint32_t m2 = min(s.live_cursor, (uint32_t)kRowsLive);
-        ok = rows_sort_list(src, s, (int)m2, (int)min(w2, m2), (int)nfin, rbase, os, oi);
+        off = (int)nfin;
+        ok = list_sort<NT, 12, kRowsLive>(ls, (int)m2, (int)min(w2, m2), out_at);
       }
       if (ok) {
         for (int j = (int)(nfin + w2) + tid; j < ksel; j += NT) {
