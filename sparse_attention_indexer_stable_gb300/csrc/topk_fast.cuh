@@ -186,7 +186,7 @@ __device__ __forceinline__ void tma_load_1d(void* smem_dst, const void* gmem_src
 // out: every slot gets id DCP_ID_UNWRITTEN and a NaN score, so that a
 // caller who does not check the device status cannot mistake stale memory
 // for a result.  Every thread of the CTA calls it.
-__device__ __noinline__ void mark_rows_unwritten(float* out_scores, int32_t* out_ids, int t, int T,
+__device__ __forceinline__ void mark_rows_unwritten(float* out_scores, int32_t* out_ids, int t, int T,
                                                  int G, int K) {
   for (; t < T; t += G) {
     float* os = out_scores + (size_t)t * (size_t)K;

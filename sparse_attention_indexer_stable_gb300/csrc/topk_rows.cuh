@@ -1,5 +1,5 @@
 // topk_rows.cuh -- the many-row merge at K = 2048 (prefill-scale merges: more
-// rows than SMs, dcp <= 4 shards of 2048 candidates each).
+// than two rows per SM, dcp <= 4 shards of 2048 candidates each).
 //
 // Four 256-thread CTAs share an SM, each walking the rows
 // t = blockIdx.x + k*gridDim.x (the 1024-row chunks of "Reserve the sparse

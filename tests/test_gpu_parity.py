@@ -158,16 +158,20 @@ CASES = [
     (3, 4, 4096, "ties", 0.8),        # K up to 4096
     (3, 8, 2048, "normal", 0.9),      # 16384 candidates per row
     (5, 4, 1024, "const", 0.9),
-    # the many-row merge at K = 2048 (more rows than SMs, four CTAs per SM)
-    (153, 4, 2048, "cluster", 0.0),   # buckets too large: the fallback's radix select
-    (170, 2, 2048, "wide", 0.0),      # ids over all of int32: 64-bit rank keys
-    (300, 4, 2048, "normal", 0.0),    # fp32 scores: 64-bit rank keys
-    (160, 4, 2048, "const", 0.0),     # one score: the id decides everything
-    (161, 4, 2048, "neginf", 0.0),    # real -inf candidates among the winners
+    # the many-row merge at K = 2048 (more than two rows per SM, four CTAs
+    # per SM)
+    (305, 4, 2048, "cluster", 0.0),   # buckets too large: the fallback's radix select
+    (330, 2, 2048, "wide", 0.0),      # ids over all of int32: 64-bit rank keys
+    (400, 4, 2048, "normal", 0.0),    # fp32 scores: 64-bit rank keys
+    (320, 4, 2048, "const", 0.0),     # one score: the id decides everything
+    (321, 4, 2048, "neginf", 0.0),    # real -inf candidates among the winners
     (611, 3, 2048, "bf16", 0.1),      # several rows per CTA, padding in some slots
-    (200, 4, 2048, "narrow", 0.3),
-    (155, 2, 2048, "ties", 0.5),
-    (157, 1, 2048, "zeros", 0.0),
+    (420, 4, 2048, "narrow", 0.3),    # bin b1 refined on the next key bits
+    (335, 2, 2048, "ties", 0.5),
+    (337, 1, 2048, "zeros", 0.0),
+    (700, 4, 2048, "bf16", 0.8),      # fewer real candidates than K: list sorts + padding
+    (650, 4, 2048, "normal", 0.95),
+    (310, 4, 2048, "neginf", 0.7),    # real -inf winners ranked by id
 ]
 
 
@@ -553,7 +557,7 @@ def test_graph_captured_prefill_chunks():
     assert_same((out_ids.cpu().numpy()[rows], out_scores.cpu().numpy()[rows]), want, "per chunk")
 
 
-@pytest.mark.parametrize("T", [16, 300])
+@pytest.mark.parametrize("T", [16, 300, 640])
 def test_masked_sweep_merge(T):
     """The merge of the local top-Ks of causally masked rows (rows of
     differing context length): shards seeing fewer than K tokens contribute

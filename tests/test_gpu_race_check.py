@@ -83,9 +83,11 @@ def test_race_check_tieheavy(rlib, seed):
     _check_merge(rlib, workloads.tieheavy(seed=100 + seed), f"seed {seed}")
 
 
-def test_race_check_prefill_slice(rlib):
-    """300 prefill rows: the many-row merge, several rows per CTA."""
-    _check_merge(rlib, workloads.prefill(T=300), "prefill 300")
+@pytest.mark.parametrize("T", [300, 700])
+def test_race_check_prefill_slice(rlib, T):
+    """Prefill rows: two 512-thread CTAs per SM (300 rows) and the many-row
+    merge's four 256-thread CTAs per SM (700 rows), several rows per CTA."""
+    _check_merge(rlib, workloads.prefill(T=T), f"prefill {T}")
 
 
 RACE_CASES = [
@@ -101,6 +103,12 @@ RACE_CASES = [
     (3, 4, 4096, "ties", 0.3),        # K up to 4096
     (6, 3, 1001, "ties", 0.1),        # the general path (K not a multiple of 4)
     (160, 4, 2048, "neginf", 0.7),
+    # the many-row merge (more than two rows per SM)
+    (700, 4, 2048, "bf16", 0.8),      # list sorts of the real candidates, padding after
+    (420, 4, 2048, "narrow", 0.0),    # refinement
+    (340, 4, 2048, "cluster", 0.0),   # the radix-select fallback
+    (400, 4, 2048, "normal", 0.0),    # 64-bit rank keys
+    (350, 4, 2048, "neginf", 0.7),    # real -inf winners ranked by id
 ]
 
 

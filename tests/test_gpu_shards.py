@@ -36,8 +36,9 @@ SHARD_CASES = [
     # (T, dcp, K, mode, pad_frac): the launch configuration they reach
     (16, 4, 2048, "normal", 0.0),     # one 1024-thread CTA per row
     (8, 4, 2048, "ties", 0.3),
-    (300, 4, 2048, "bf16", 0.0),      # the many-row merge, four CTAs per SM
-    (160, 3, 2048, "bf16", 0.8),      # many rows, padding-heavy
+    (400, 4, 2048, "bf16", 0.0),      # the many-row merge, four CTAs per SM
+    (330, 3, 2048, "bf16", 0.8),      # the same, padding-heavy
+    (160, 4, 2048, "normal", 0.0),    # two 512-thread CTAs per SM
     (200, 2, 1024, "ties", 0.1),      # two 512-thread CTAs per SM
     (5, 3, 1001, "normal", 0.1),      # K not a multiple of 4: the general path
     (3, 8, 2048, "normal", 0.0),      # 16384 candidates per row
@@ -99,7 +100,7 @@ def test_merge_shards_graph_replay_repointed():
     assert np.array_equal(_bits(os_.cpu().numpy()), _bits(ws))
 
 
-@pytest.mark.parametrize("T", [16, 300])
+@pytest.mark.parametrize("T", [16, 300, 400])
 def test_merge_shards_misaligned_is_reported(T):
     """A shard 4 bytes off a 16-byte boundary (K % 4 == 0): the kernel checks
     the pointers before reading any shard, reports
