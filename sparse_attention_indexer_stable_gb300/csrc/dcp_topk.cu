@@ -423,16 +423,17 @@ static cudaError_t allow_max_smem(K kernel, int bytes) {
 template <class Source>
 static cudaError_t allow_stream_kernels(int smem) {
   cudaError_t e;
-  if ((e = allow_max_smem(topk_stream_kernel<512, kStreamMaxN, kStreamMaxK, Source>, smem)) !=
-      cudaSuccess)
-    return e;
-  if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxN, kStreamMaxK, Source>, smem)) !=
-      cudaSuccess)
-    return e;
-  if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxK, Source>,
+  if ((e = allow_max_smem(topk_stream_kernel<512, kStreamMaxN, kStreamMaxK, Source, false>,
                           smem)) != cudaSuccess)
     return e;
-  return allow_max_smem(topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxKWide, Source>, smem);
+  if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxN, kStreamMaxK, Source, true>,
+                          smem)) != cudaSuccess)
+    return e;
+  if ((e = allow_max_smem(topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxK, Source, true>,
+                          smem)) != cudaSuccess)
+    return e;
+  return allow_max_smem(
+      topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxKWide, Source, true>, smem);
 }
 
 // Per-device launch limits and kernel attributes, set once per device (the
@@ -483,10 +484,10 @@ static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // access) before touching memory.  Only the launch latency and shared-memory
 // set-up overlap; the ordering is the stream's.
 template <typename... KArgs, typename... Args>
-static cudaError_t launch_serialized(void (*kernel)(KArgs...), int grid, int block, size_t smem,
+static cudaError_t launch_serialized(void (*kernel)(KArgs...), dim3 grid, int block, size_t smem,
                                      cudaStream_t stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3((unsigned)block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -536,6 +537,17 @@ static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out
   const bool stream_ok = src.vec4 && K <= kStreamMaxKWide && n <= kStreamMaxNWide &&
                          smem <= (size_t)d->max_smem_optin;
   const int grid1 = T < d->sms ? T : d->sms;
+  // Few rows: each row's sort split over up to 8 CTAs (parts, the grid's y
+  // dimension), every part selecting the whole row's threshold and sorting a
+  // slice of at least 256 of its min(K, n) winners, while the parts fit on
+  // the SMs at once.
+  const int ksel = K < n ? K : n;
+  int parts = T > 0 ? d->sms / T : 1;
+  parts = parts < 8 ? parts : 8;
+  parts = parts < ksel / 256 ? parts : ksel / 256;
+  parts = parts > 1 ? parts : 1;
+  const dim3 gridp((unsigned)grid1, (unsigned)parts);  // T * parts <= sms when parts > 1
+  const int slice = ksel / parts;
   cudaError_t e;
   if constexpr (Source::kMerge) {
     // above two rows per SM (at or below, the streaming kernel's two
@@ -549,18 +561,20 @@ static dcp_status launch_rows(const Source& src, int T, int n, int K, float* out
     }
   }
   if (stream_ok && big_k) {
-    e = launch_serialized(topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxKWide, Source>,
-                          grid1, 1024, smem, stream, src, T, K, out_scores, out_ids, d->status);
+    e = launch_serialized(
+        topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxKWide, Source, true>, gridp, 1024,
+        smem, stream, src, T, K, slice, out_scores, out_ids, d->status);
   } else if (stream_ok && n > kStreamMaxN) {
-    e = launch_serialized(topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxK, Source>, grid1,
-                          1024, smem, stream, src, T, K, out_scores, out_ids, d->status);
+    e = launch_serialized(topk_stream_kernel<1024, kStreamMaxNWide, kStreamMaxK, Source, true>,
+                          gridp, 1024, smem, stream, src, T, K, slice, out_scores, out_ids,
+                          d->status);
   } else if (stream_ok && !two_per_sm) {
-    e = launch_serialized(topk_stream_kernel<1024, kStreamMaxN, kStreamMaxK, Source>, grid1, 1024,
-                          smem, stream, src, T, K, out_scores, out_ids, d->status);
+    e = launch_serialized(topk_stream_kernel<1024, kStreamMaxN, kStreamMaxK, Source, true>, gridp,
+                          1024, smem, stream, src, T, K, slice, out_scores, out_ids, d->status);
   } else if (stream_ok) {
     const int grid = T < 2 * d->sms ? T : 2 * d->sms;
-    e = launch_serialized(topk_stream_kernel<512, kStreamMaxN, kStreamMaxK, Source>, grid, 512,
-                          smem, stream, src, T, K, out_scores, out_ids, d->status);
+    e = launch_serialized(topk_stream_kernel<512, kStreamMaxN, kStreamMaxK, Source, false>, grid,
+                          512, smem, stream, src, T, K, 1, out_scores, out_ids, d->status);
   } else {
     const size_t gsmem = row_smem_bytes(n, K);
     if (gsmem > (size_t)d->max_smem_optin) return DCP_ERR_UNSUPPORTED;

@@ -109,11 +109,13 @@ struct StreamShared {
   uint32_t stat_and[2];               // [1]: AND of ~ids (not 0)
   uint32_t live_cursor;
   uint32_t b1;                        // L1 bin of the K-th largest key
-  uint32_t nlive;                     // candidates in bins >= b1
-  uint32_t nfine;                     // fine buckets of bins >= b1
   uint32_t above_b1;                  // candidates in bins above b1
   uint32_t found_digit, found_above, found_count;  // refinement of b1
-  uint32_t p_end;                     // end of the bucket straddling K
+  uint32_t p_end;                     // end of the bucket straddling the slice's end
+  uint32_t p_begin;                   // start of the bucket straddling the slice's start
+  uint32_t part_bh, part_bl;          // the slice's highest and lowest L1 bins
+  uint32_t part_pmin, part_fmin;      // the first position and fine bucket of bin part_bh
+  uint32_t part_pend, part_fend;      // the end position and fine bucket of bin part_bl
   uint32_t overflow;                  // a bucket to rank is too large
   uint32_t pad_n;                     // fallback: padding keys of the row
   uint32_t lscal[8];                  // list_sort's scalars
@@ -717,9 +719,16 @@ __device__ __noinline__ void fallback_row(const Source src, Shared& s, const uin
   }
 }
 
-template <int NT, int MAXN, int KMAX, class Source>
+// kSplit: the grid's y dimension splits each row's sort into gridDim.y
+// parts.  Part y (a CTA of its own) stages the whole row and selects its
+// threshold bin (the same in every part), then sorts only the bins whose
+// output positions meet its slice [y*slice, (y+1)*slice) of the
+// k = min(K, n) winners (the last part's slice ending at k) and writes that
+// slice.  The slices partition the output, so a row's result does not
+// depend on the split.
+template <int NT, int MAXN, int KMAX, class Source, bool kSplit>
 __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
-    topk_stream_kernel(Source src, int T, int K, float* __restrict__ out_scores,
+    topk_stream_kernel(Source src, int T, int K, int slice, float* __restrict__ out_scores,
                        int32_t* __restrict__ out_ids, unsigned int* __restrict__ status) {
   constexpr int kWarpsT = NT / 32;
   constexpr int kVec = MAXN / 4 / NT;  // 16-byte score chunks per thread
@@ -756,7 +765,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   zero_words<NT>(s.fine, kFineMax + kL1Bins);  // fine and the table behind it
   if (tid == 0) {
     s.live_cursor = 0u;
-    s.p_end = 0u;
+    s.p_end = s.p_begin = 0u;
     s.overflow = 0u;
     s.pad_n = 0u;
     s.stat_or[0] = s.stat_or[1] = 0u;
@@ -768,6 +777,10 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   // visits exactly this sequence.
   const int G = (int)gridDim.x;
   int t = (int)blockIdx.x;
+  // this part's output slice [lo, hi)
+  const uint32_t lo = kSplit ? blockIdx.y * (uint32_t)slice : 0u;
+  const uint32_t hi =
+      kSplit && blockIdx.y + 1u < gridDim.y ? lo + (uint32_t)slice : (uint32_t)ksel;
   if (tid == 0) {
     mbar_init(&s.stage_bar, 1u);
     mbar_init(&s.ids_bar, 1u);
@@ -876,9 +889,18 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
           if (h[e] != 0u) {
             if (above < (uint32_t)ksel && (uint32_t)ksel <= above + h[e]) {
               s.b1 = (uint32_t)b;
-              s.nlive = above + h[e];
-              s.nfine = fabove + f[e];
               s.above_b1 = above;
+            }
+            // the bins holding the slice's first and last positions
+            if (kSplit && above <= lo && lo < above + h[e]) {
+              s.part_bh = (uint32_t)b;
+              s.part_pmin = above;
+              s.part_fmin = fabove;
+            }
+            if (above < hi && hi <= above + h[e]) {
+              s.part_bl = (uint32_t)b;
+              s.part_pend = above + h[e];
+              s.part_fend = fabove + f[e];
             }
             s.u.table[b] = (fabove << 8) | (uint32_t)(31 - __clz(f[e]));
           }
@@ -903,14 +925,20 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     }
 
     const uint32_t b1 = s.b1;
-    const int nfine = (int)s.nfine;
-    // Live candidates are those with (key >> kRefShift) >= live_from.
-    // Normally that is every candidate of bins >= b1; when the live set would
-    // overflow the live list, the next 11 key bits of bin b1 are histogrammed
-    // (in `fine`, still zero) and only its candidates from the digit holding
-    // the K-th key on are kept live.
-    uint32_t live_from = b1 << 11;
-    if (s.nlive > (uint32_t)kLiveMax) {
+    // The slice's bins are [bl, bh] (all bins >= b1 without a split); their
+    // positions start at pmin and their fine buckets at fmin, which the
+    // slice's lists and buckets count from.
+    const uint32_t bh = kSplit ? s.part_bh : 0u, bl = s.part_bl;
+    const uint32_t pmin = kSplit ? s.part_pmin : 0u, fmin = kSplit ? s.part_fmin : 0u;
+    const int nfine = (int)(s.part_fend - fmin);
+    uint32_t nlv = s.part_pend - pmin;  // the slice's live candidates
+    // Live candidates are those with bin <= bh and (key >> kRefShift) >=
+    // live_from.  Normally that is every candidate of bins [bl, bh]; when the
+    // live set would overflow the live list and bl is b1, the next 11 key
+    // bits of bin b1 are histogrammed (in `fine`, still zero) and only its
+    // candidates from the digit holding the K-th key on are kept live.
+    uint32_t live_from = bl << 11;
+    if (nlv > (uint32_t)kLiveMax && bl == b1) {
 #pragma unroll
       for (int j = 0; j < kItems; ++j) {
         if ((tid + (j >> 2) * NT) < n4 && (keys[j] >> kL1Shift) == b1)
@@ -921,7 +949,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
                           s.found_above, s.found_count);
       row_sync();
       live_from |= s.found_digit;
-      const uint32_t nl = s.above_b1 + s.found_above + s.found_count;
+      nlv = s.above_b1 + s.found_above + s.found_count - pmin;
       if constexpr (kPoisonBuild) {
         row_sync();
         dbg_poison<NT>(s.fine, kHistBins);
@@ -929,23 +957,30 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       }
       zero_words<NT>(s.fine, kHistBins);  // the refinement histogram: 2048 words of fine
       row_sync();
-      if (tid == 0) s.nlive = nl;
-      row_sync();
     }
-    const int nlive = (int)s.nlive;
+    const int nlive = (int)nlv;
     bool fast = nlive <= kLiveMax;
 
     // ---- COMPACT: live candidates into a dense list -------------------------
     if (fast) {
       uint32_t mask = 0u;
-      const uint32_t lf = live_from << kRefShift;  // live: key >= lf
+      const uint32_t lf = live_from << kRefShift;  // live: key >= lf (and bin <= bh)
+      // kSplit: key - lf < span <=> lf <= key < (bh + 1) << kL1Shift (mod 2^32)
+      const uint32_t span = ((bh + 1u) << kL1Shift) - lf;
       if (lf != 0u) {
         // candidates past the row hold key 0 (< lf)
+        if constexpr (kSplit) {
 #pragma unroll
-        for (int j = 0; j < kItems; ++j) mask |= (keys[j] >= lf ? 1u : 0u) << j;
+          for (int j = 0; j < kItems; ++j) mask |= (keys[j] - lf < span ? 1u : 0u) << j;
+        } else {
+#pragma unroll
+          for (int j = 0; j < kItems; ++j) mask |= (keys[j] >= lf ? 1u : 0u) << j;
+        }
       } else {
 #pragma unroll
-        for (int j = 0; j < kItems; ++j) mask |= ((tid + (j >> 2) * NT) < n4 ? 1u : 0u) << j;
+        for (int j = 0; j < kItems; ++j)
+          mask |= ((tid + (j >> 2) * NT) < n4 && (!kSplit || (keys[j] >> kL1Shift) <= bh) ? 1u : 0u)
+                  << j;
       }
       const uint32_t cnt = __popc(mask);
       const uint32_t incl = warp_inclusive_scan(cnt);
@@ -1018,7 +1053,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
             w = kL1Shift + 32;
           }
           const uint32_t sub = w >= q ? (uint32_t)(y >> (w - q)) : (uint32_t)(y << (q - w));
-          const uint32_t g = (tb >> 8) + ((1u << q) - 1u - sub);
+          const uint32_t g = (tb >> 8) + ((1u << q) - 1u - sub) - fmin;
           atomicAdd(&s.fine[dbg_clamp(g, kFineMax)], 1u);
           gslot[u] = dbg_clamp(g, kFineMax);
         }
@@ -1060,12 +1095,15 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         uint32_t st = __shfl_sync(0xFFFFFFFFu, wti - wt, warp) + incl - local;
         uint32_t over = 0u;
         uint32_t w[kFinePer];
+        // the slice's positions, counted from pmin
+        const uint32_t klo = lo - pmin, khi = hi - pmin;
 #pragma unroll
         for (int e = 0; e < kFinePer; ++e) {
           w[e] = (st << 16) | (min(c[e], 255u) << 8);
-          if (st < (uint32_t)ksel) {
+          if (st < khi && (!kSplit || klo < st + c[e])) {
             if (c[e] > kBigBucket) over = 1u;
-            if ((uint32_t)ksel <= st + c[e]) s.p_end = st + c[e];
+            if (khi <= st + c[e]) s.p_end = st + c[e];
+            if (kSplit && st <= klo) s.p_begin = st;
           }
           st += c[e];
         }
@@ -1095,12 +1133,15 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       // 11 or 12 bits (the L1 bin), so dropping 11 of them keeps the key order
       // within the bucket, identical keys told apart by their slot (the
       // smaller slot first).
+      const uint32_t klo = lo - pmin, khi = hi - pmin;
+      const uint32_t p_begin = kSplit ? s.p_begin : 0u;
 #pragma unroll
       for (int u = 0; u < kLivePer; ++u) {
         if (gslot[u] != kNone) {
           const uint32_t old = atomicAdd(&s.fine[gslot[u]], 1u);
-          if ((old >> 16) < (uint32_t)ksel) {
-            const uint32_t pos = dbg_clamp((old >> 16) + (old & 0xFFu), kRankMax);
+          // buckets meeting the slice, listed from the one holding its start
+          if ((old >> 16) < khi && (!kSplit || klo < (old >> 16) + ((old >> 8) & 0xFFu))) {
+            const uint32_t pos = dbg_clamp((old >> 16) - p_begin + (old & 0xFFu), kRankMax);
             s.live[pos] = lkey[u];
             info[pos] = (uint16_t)(old & 0xFFFFu);
             if (((old >> 8) & 0xFFu) > 1u) rkl[pos] = (lkey[u] << 11) | (255u - (old & 0xFFu));
@@ -1112,8 +1153,9 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       // ---- RANK: position = bucket start + members ranking above ----------
       // Per list position.  Consecutive positions share buckets, so a warp's
       // buckets are usually all small enough for a 4-wide window.
-      const uint32_t p_end = min(s.p_end, (uint32_t)kRankMax);
+      const uint32_t p_end = min(s.p_end - p_begin, (uint32_t)kRankMax);
       const uint32_t rbase = src.row_base(t);
+      const uint32_t p_off = pmin + p_begin;  // output position of list position 0
       for (uint32_t p = tid; p < p_end; p += NT) {
         const uint32_t inf = info[p];
         const uint32_t st = dbg_clamp(p - (inf & 0xFFu), p + 1u);
@@ -1136,15 +1178,17 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
             for (uint32_t e = 0; e < cnt; ++e) r += b[e] > mine ? 1u : 0u;
           }
         }
-        const uint32_t fin = st + r;
-        if (fin < (uint32_t)ksel) {
+        const uint32_t fin = p_off + st + r;
+        if ((!kSplit || lo <= fin) && fin < hi) {
           os[fin] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
           oi[fin] = src.out_id_from(rbase, (uint32_t)key);
         }
       }
-      for (int j = ksel + tid; j < K; j += NT) {
-        os[j] = __uint_as_float(0xFF800000u);  // -inf
-        oi[j] = -1;
+      if (!kSplit || blockIdx.y + 1u == gridDim.y) {
+        for (int j = ksel + tid; j < K; j += NT) {
+          os[j] = __uint_as_float(0xFF800000u);  // -inf
+          oi[j] = -1;
+        }
       }
     } else {
       fallback_row<NT, KMAX>(src, s, aux, t, n, ksel, K, os, oi);
@@ -1162,7 +1206,9 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       dbg_poison<NT>(s.wa, 2 * kMaxWarps);
       if constexpr (!Source::kStagesIds) dbg_poison<NT>(aux, Caps::kScratchWords);
       if (tid == 0) {
-        s.b1 = s.nlive = s.nfine = s.above_b1 = 0xA5A5A5A5u;
+        s.b1 = s.above_b1 = 0xA5A5A5A5u;
+        s.part_bh = s.part_bl = s.part_pmin = s.part_fmin = 0xA5A5A5A5u;
+        s.part_pend = s.part_fend = 0xA5A5A5A5u;
         s.found_digit = s.found_above = s.found_count = 0xA5A5A5A5u;
       }
       __syncthreads();
@@ -1170,7 +1216,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     zero_words<NT>(s.fine, kFineMax + kL1Bins);  // fine and the table behind it
     if (tid == 0) {
       s.live_cursor = 0u;
-      s.p_end = 0u;
+      s.p_end = s.p_begin = 0u;
       s.overflow = 0u;
       s.pad_n = 0u;
       s.stat_or[0] = s.stat_or[1] = 0u;

@@ -141,6 +141,7 @@ CASES = [
     # every candidate in one L1 bin: the live set is refined on the next bits
     (200, 4, 2048, "narrow", 0.0),    # two CTAs per SM
     (8, 4, 2048, "narrow", 0.0),      # one CTA per row
+    (100, 4, 2048, "narrow", 0.0),
     (3, 4, 4096, "narrow", 0.0),      # K up to 4096
     # K above 2048: the one-CTA-per-row instantiation for K up to 4096
     (5, 2, 4096, "zeros", 0.0),
@@ -151,6 +152,9 @@ CASES = [
     (2, 4, 3072, "wide", 0.0),
     # fewer real candidates than K (short shards): the K-th key is padding
     (16, 4, 2048, "normal", 0.8),     # one CTA per row
+    (120, 4, 2048, "normal", 0.8),
+    (90, 4, 2048, "cluster", 0.0),    # the same, buckets too large
+    (110, 4, 2048, "neginf", 0.0),
     (200, 4, 2048, "bf16", 0.8),      # two CTAs per SM
     (200, 4, 2048, "normal", 0.95),
     (4, 4, 2048, "neginf", 0.8),      # real -inf candidates above the padding
@@ -158,6 +162,14 @@ CASES = [
     (3, 4, 4096, "ties", 0.8),        # K up to 4096
     (3, 8, 2048, "normal", 0.9),      # 16384 candidates per row
     (5, 4, 1024, "const", 0.9),
+    # few rows: each row's sort split over parts = min(8, SMs / T) CTAs,
+    # slices of the output not all of one size
+    (20, 4, 2048, "bf16", 0.0),       # 7 parts
+    (25, 4, 2048, "ties", 0.2),       # 6 parts
+    (30, 3, 2048, "normal", 0.5),     # 5 parts, padding in the last slices
+    (45, 8, 2048, "narrow", 0.0),     # 3 parts, 16384 candidates, b1 refined
+    (7, 4, 4096, "bf16", 0.0),        # 8 parts of K = 4096
+    (2, 4, 2048, "cluster", 0.3),     # 8 parts, oversized buckets in some slices
     # the many-row merge at K = 2048 (more than two rows per SM, four CTAs
     # per SM)
     (305, 4, 2048, "cluster", 0.0),   # buckets too large: the fallback's radix select

@@ -94,10 +94,18 @@ RACE_CASES = [
     # (T, dcp, K, mode, pad_frac)
     (200, 4, 2048, "bf16", 0.8),      # many rows, fewer real candidates than K: the fallback
     (16, 4, 2048, "normal", 0.8),     # one CTA per row, the same
+    (120, 4, 2048, "normal", 0.8),
     (200, 4, 2048, "narrow", 0.0),    # the live set refined on the next key bits
     (8, 4, 2048, "narrow", 0.0),
+    (100, 4, 2048, "narrow", 0.0),
     (153, 4, 2048, "cluster", 0.0),   # buckets too large: the radix-select fallback
     (5, 4, 2048, "cluster", 0.0),
+    (90, 4, 2048, "cluster", 0.0),
+    (16, 4, 2048, "neginf", 0.0),     # real -inf candidates below the winners
+    (38, 4, 2048, "bf16", 0.1),
+    (50, 4, 2048, "ties", 0.3),
+    (8, 8, 2048, "bf16", 0.0),        # 16384 candidates per row
+    (16, 4, 2048, "wide", 0.0),
     (300, 4, 2048, "normal", 0.0),    # fp32 scores: 64-bit rank keys
     (170, 2, 1024, "ties", 0.1),      # two 512-thread CTAs per SM
     (3, 4, 4096, "ties", 0.3),        # K up to 4096

@@ -35,6 +35,7 @@ def _shards(m):
 SHARD_CASES = [
     # (T, dcp, K, mode, pad_frac): the launch configuration they reach
     (16, 4, 2048, "normal", 0.0),     # one 1024-thread CTA per row
+    (100, 4, 2048, "normal", 0.0),
     (8, 4, 2048, "ties", 0.3),
     (400, 4, 2048, "bf16", 0.0),      # the many-row merge, four CTAs per SM
     (330, 3, 2048, "bf16", 0.8),      # the same, padding-heavy
