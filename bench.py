@@ -196,6 +196,28 @@ def median_of_reps(torch, fn, stream, reps=7, launches=200, graph=False):
     return statistics.median(out[1:])
 
 
+def cold_launch_us(torch, fn, stream, reps=21):
+    """Median device time (µs) of single launches with the L2 flushed before
+    each (a 256 MiB write, twice the 129 MB L2), so that the inputs come from
+    HBM.  The flush, the start event, the launch and the end event are queued
+    together: the flush keeps the stream busy while the host queues the rest,
+    so the interval holds the launch alone, not the host's launch latency."""
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=stream.device)
+    out = []
+    for _ in range(reps + 1):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        b.synchronize()
+        out.append(a.elapsed_time(b) * 1000.0)
+    del flush
+    return statistics.median(out[1:])
+
+
 def replica_throughput(torch, local_ms, rows_per_step, steps, dist=None, device=None):
     """Whole-job rows/s over the ranks of a replicas-only run: every rank
     processed rows_per_step * steps rows; the job took the slowest rank's
@@ -459,6 +481,7 @@ def decode_and_sweep(torch, dk, dev, stream):
         out[f"{name}_T{m.T}_us_per_launch"] = median_of_reps(torch, raw, stream)
         out[f"{name}_T{m.T}_us_per_graph_replay"] = median_of_reps(torch, raw, stream, graph=True)
         out[f"{name}_T{m.T}_us_per_python_call"] = median_of_reps(torch, fn, stream)
+        out[f"{name}_T{m.T}_us_cold"] = cold_launch_us(torch, raw, stream)
     # the selector shapes of the first page's table (K=2048; candidates dcp*K;
     # random fp32 scores), timed like the decode merge
     shapes = {}

@@ -985,7 +985,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       const uint32_t cnt = __popc(mask);
       const uint32_t incl = warp_inclusive_scan(cnt);
       uint32_t base = 0u;
-      if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
+      if (lane == 31 && incl != 0u) base = atomicAdd(&s.live_cursor, incl);  // warps with live keys
       unsigned long long* dst =
           s.live + dbg_clamp(__shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt, kLiveMax + 1u - cnt);
       // OR / AND of the inverted ids around the live candidates (padding's
