@@ -218,6 +218,26 @@ def cold_launch_us(torch, fn, stream, reps=21):
     return statistics.median(out[1:])
 
 
+def cold_inputs_launch_us(torch, fns, stream):
+    """Median device time (µs) of single launches whose inputs are not in L2:
+    fns[i] runs on its own copy of the inputs, the copies together larger
+    than L2 and used in turn, so each launch reads its inputs from HBM while
+    the kernel's code stays cached.  The launches are queued together, each
+    between two events (which also keeps it from overlapping its neighbours),
+    so no interval holds the host's launch latency."""
+    evs = []
+    with torch.cuda.stream(stream):
+        for fn in fns:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+    stream.synchronize()
+    return statistics.median(a.elapsed_time(b) * 1000.0 for a, b in evs[len(evs) // 2:])
+
+
 def replica_throughput(torch, local_ms, rows_per_step, steps, dist=None, device=None):
     """Whole-job rows/s over the ranks of a replicas-only run: every rank
     processed rows_per_step * steps rows; the job took the slowest rank's
@@ -481,7 +501,15 @@ def decode_and_sweep(torch, dk, dev, stream):
         out[f"{name}_T{m.T}_us_per_launch"] = median_of_reps(torch, raw, stream)
         out[f"{name}_T{m.T}_us_per_graph_replay"] = median_of_reps(torch, raw, stream, graph=True)
         out[f"{name}_T{m.T}_us_per_python_call"] = median_of_reps(torch, fn, stream)
-        out[f"{name}_T{m.T}_us_cold"] = cold_launch_us(torch, raw, stream)
+        # single launches on inputs from HBM (200 copies of the 1 MiB of
+        # candidates, cycled twice), and with the whole L2 flushed, code too
+        copies = [(s.clone(), i.clone()) for _ in range(200)]
+        fns = [(lambda a=(sc.data_ptr(), ic.data_ptr(), m.T, m.dcp, m.K, None, oi.data_ptr(),
+                           os_.data_ptr(), None, 0, stream.cuda_stream): lib.dcp_topk_merge(*a))
+               for sc, ic in copies * 2]
+        out[f"{name}_T{m.T}_us_cold_inputs"] = cold_inputs_launch_us(torch, fns, stream)
+        del copies, fns
+        out[f"{name}_T{m.T}_us_cold_l2_flushed"] = cold_launch_us(torch, raw, stream)
     # the selector shapes of the first page's table (K=2048; candidates dcp*K;
     # random fp32 scores), timed like the decode merge
     shapes = {}

@@ -988,29 +988,45 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       if (lane == 31 && incl != 0u) base = atomicAdd(&s.live_cursor, incl);  // warps with live keys
       unsigned long long* dst =
           s.live + dbg_clamp(__shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt, kLiveMax + 1u - cnt);
-      // OR / AND of the inverted ids around the live candidates (padding's
-      // ~id of 0 left out: it is the smallest, so ordering on the varying
-      // bits alone still puts it last)
-      uint32_t ior = 0u, iand = 0xFFFFFFFFu;
+      if constexpr (Source::kStagesIds) {
+        // OR / AND of the inverted ids around the live candidates (padding's
+        // ~id of 0 left out: it is the smallest, so ordering on the varying
+        // bits alone still puts it last)
+        uint32_t ior = 0u, iand = 0xFFFFFFFFu;
 #pragma unroll
-      for (int v = 0; v < kVec; ++v) {
-        if ((tid + v * NT) < n4) {
-          const uint4 u4 = src.inv4(aux, tid + v * NT);
-          const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
+        for (int v = 0; v < kVec; ++v) {
+          if ((tid + v * NT) < n4) {
+            const uint4 u4 = src.inv4(aux, tid + v * NT);
+            const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            ior |= us[e];
-            iand &= us[e] ? us[e] : 0xFFFFFFFFu;
-            if (mask & (1u << (4 * v + e)))
-              *dst++ = ((unsigned long long)keys[4 * v + e] << 32) | us[e];
+            for (int e = 0; e < 4; ++e) {
+              ior |= us[e];
+              iand &= us[e] ? us[e] : 0xFFFFFFFFu;
+              if (mask & (1u << (4 * v + e)))
+                *dst++ = ((unsigned long long)keys[4 * v + e] << 32) | us[e];
+            }
           }
         }
-      }
-      ior = __reduce_or_sync(0xFFFFFFFFu, ior);
-      iand = __reduce_and_sync(0xFFFFFFFFu, iand);
-      if (lane == 0) {
-        atomicOr(&s.stat_or[1], ior);
-        atomicAnd(&s.stat_and[1], iand);
+        ior = __reduce_or_sync(0xFFFFFFFFu, ior);
+        iand = __reduce_and_sync(0xFFFFFFFFu, iand);
+        if (lane == 0) {
+          atomicOr(&s.stat_or[1], ior);
+          atomicAnd(&s.stat_and[1], iand);
+        }
+      } else {
+        // ids computed from the candidate index (below n): only the live
+        // candidates' are formed; their statistics are known (L2)
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+          if (((mask >> (4 * v)) & 0xFu) != 0u) {
+            const uint4 u4 = src.inv4(aux, tid + v * NT);
+            const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (mask & (1u << (4 * v + e)))
+                *dst++ = ((unsigned long long)keys[4 * v + e] << 32) | us[e];
+          }
+        }
       }
     }
     row_sync();
@@ -1026,7 +1042,11 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       // wf-bit number whose top q bits name the bucket.  Bins up to kPadBin
       // (-inf, where padding lives, and below) keep every bit.
       const uint32_t ro = s.stat_or[0];
-      const uint32_t vi = s.stat_or[1] ^ s.stat_and[1];
+      // ~id bits that vary: measured in COMPACT, or, for ids computed from
+      // the candidate index i < n, the low bits of n - 1 (~i agrees above them)
+      const uint32_t vi = Source::kStagesIds ? s.stat_or[1] ^ s.stat_and[1]
+                          : n > 1            ? 0xFFFFFFFFu >> __clz(n - 1)
+                                             : 0u;
       const int tzf = ro ? min(__ffs(ro) - 1, kL1Shift) : kL1Shift;
       const int ibf = vi ? 32 - __clz(vi) : 0;
       const uint32_t imask = ibf >= 32 ? 0xFFFFFFFFu : ((1u << ibf) - 1u);

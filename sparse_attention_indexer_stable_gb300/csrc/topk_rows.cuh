@@ -66,6 +66,7 @@ constexpr int kRowsRankMax = kRowsK + 256;  // list positions: up to the end of 
 constexpr int kRowsRankWords = (kRowsRankMax + 8) * 2;  // 64-bit rank keys, + a window's overrun
 constexpr int kRowsRegionWords = kRowsRankWords + kRowsRankMax / 2;  // + u16 bucket info
 constexpr uint32_t kRowsPadBin = kNegInfKey >> kRowsL1Shift;  // bin of -inf keys (padding)
+constexpr int kRowsInfIds = kRowsFine + kRowsRegionWords;     // fallback: ~ids of -inf candidates
 
 struct RowsShared {
   uint32_t fine[kRowsFine];            // L2 bucket sizes, then start << 16 | size << 8 | fill cursor
@@ -94,6 +95,9 @@ static_assert(offsetof(RowsShared, region) % 16 == 0 && offsetof(RowsShared, liv
 static_assert(kRowsRegionWords >= kRowsBins, "histogram");
 static_assert(sizeof(SelectShared) <= sizeof(uint32_t) * kRowsRegionWords, "fallback state");
 static_assert(kRowsLive >= kRowsK && kRowsRankMax >= kRowsK + (int)kBigBucket - 1, "caps");
+// the fallback's -inf ~ids (one per candidate) fill fine and region; its
+// radix histogram (256 words) follows at most K - 1 finite keys in live
+static_assert(kRowsInfIds >= kRowsMaxN && 2 * (kRowsK - 1) + 256 <= 2 * kRowsLive, "fallback");
 
 // Starts pulling `bytes` (a multiple of 16, 16-byte aligned) into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
@@ -120,7 +124,7 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
                                            float* os, int32_t* oi) {
   constexpr int NT = kRowsNT;
   constexpr int ksel = kRowsK;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n4 = n >> 2;
   const uint32_t rbase = src.row_base(t);
   SelectShared& sel = *reinterpret_cast<SelectShared*>(s.region);
@@ -135,14 +139,17 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
     oi[off + (int)pos] = src.out_id_from(rbase, (uint32_t)key);
   };
   if (s.b1 == kRowsPadBin) {
-    // finite candidates into the list; real -inf and padding counted
+    // One pass over the row: the finite candidates into the list, the real
+    // -inf candidates' ~ids into inf_ids (fine and region, one array of
+    // kRowsInfIds words: room for every candidate), padding counted.
+    uint32_t* inf_ids = s.fine;
     if (tid == 0) {
       s.live_cursor = 0u;
       s.pad_n = 0u;
       s.found_count = 0u;  // here: the real -inf candidates
     }
     row_sync();
-    uint32_t npad = 0u, nreal_inf = 0u;
+    uint32_t npad = 0u;
 #pragma unroll 1
     for (int c0 = 0; c0 < n4; c0 += NT) {
       const int c = c0 + tid;
@@ -154,99 +161,125 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
       }
       const uint32_t ks[4] = {k4.x, k4.y, k4.z, k4.w};
       const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
-      uint32_t fm = 0u;
+      uint32_t fm = 0u, im = 0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         if (c < n4) {
           fm |= (ks[e] > kNegInfKey ? 1u : 0u) << e;
+          im |= (ks[e] == kNegInfKey && us[e] != 0u ? 1u : 0u) << e;
           npad += (ks[e] == kNegInfKey && us[e] == 0u) ? 1u : 0u;
-          nreal_inf += (ks[e] == kNegInfKey && us[e] != 0u) ? 1u : 0u;
         }
       }
-      const uint32_t cnt = __popc(fm);
-      const uint32_t incl = warp_inclusive_scan(cnt);
-      uint32_t base = 0u;
-      if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
-      uint32_t slot = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+      const uint32_t fcnt = __popc(fm);
+      const uint32_t fincl = warp_inclusive_scan(fcnt);
+      uint32_t fbase = 0u;
+      if (lane == 31 && fincl) fbase = atomicAdd(&s.live_cursor, fincl);
+      uint32_t fslot = __shfl_sync(0xFFFFFFFFu, fbase, 31) + fincl - fcnt;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         if (fm & (1u << e)) {
-          if (slot < (uint32_t)kRowsLive) s.live[slot] = ((unsigned long long)ks[e] << 32) | us[e];
-          ++slot;
+          if (fslot < (uint32_t)kRowsLive) s.live[fslot] = ((unsigned long long)ks[e] << 32) | us[e];
+          ++fslot;
+        }
+      }
+      if (__any_sync(0xFFFFFFFFu, im != 0u)) {  // padding-only chunks skip this
+        const uint32_t icnt = __popc(im);
+        const uint32_t iincl = warp_inclusive_scan(icnt);
+        uint32_t ibase = 0u;
+        if (lane == 31) ibase = atomicAdd(&s.found_count, iincl);
+        uint32_t islot = __shfl_sync(0xFFFFFFFFu, ibase, 31) + iincl - icnt;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (im & (1u << e)) {
+            if (islot < (uint32_t)kRowsInfIds) inf_ids[islot] = us[e];
+            ++islot;
+          }
         }
       }
     }
     npad = __reduce_add_sync(0xFFFFFFFFu, npad);
-    nreal_inf = __reduce_add_sync(0xFFFFFFFFu, nreal_inf);
-    if (lane == 0) {
-      if (npad != 0u) atomicAdd(&s.pad_n, npad);
-      if (nreal_inf != 0u) atomicAdd(&s.found_count, nreal_inf);
-    }
+    if (lane == 0 && npad != 0u) atomicAdd(&s.pad_n, npad);
     row_sync();
-    const uint32_t nfin = s.live_cursor;     // finite candidates (above -inf)
-    const uint32_t rinf = s.found_count;     // real -inf candidates
-    const uint32_t npd = s.pad_n;            // padding
+    const uint32_t nfin = s.live_cursor;                        // finite candidates
+    const uint32_t rinf = min(s.found_count, (uint32_t)kRowsInfIds);  // real -inf candidates
+    const uint32_t npd = s.pad_n;                               // padding
     if (nfin < (uint32_t)ksel && nfin + rinf + npd >= (uint32_t)ksel) {
-      bool ok = list_sort<NT, 12, kRowsLive>(ls, (int)nfin, (int)nfin, out_at);
-      const uint32_t w2 = min(rinf, (uint32_t)ksel - nfin);  // -inf winners
-      if (ok && w2 > 0u) {
-        // the real -inf candidates with the lowest ids: the list holds them
-        // all, or a radix select on ~id finds the w2 largest first
-        RadixResult rr{0u, 0u, 0u, 0u};
-        const bool select = rinf > (uint32_t)kRowsLive;
-        if (select)
-          rr = radix_select<NT>(sel, n, w2, [&](int i, uint32_t& v) {
-            v = src.inv_global(t, i);
-            return v != 0u && src.key_global(t, i) == kNegInfKey;
-          });
-        if (tid == 0) {
-          s.live_cursor = 0u;
-          sel.dup_claim = 0u;
-        }
-        row_sync();
+      // The -inf winners: the w2 real -inf candidates with the lowest ids,
+      // i.e. the largest ~ids.  With more of them than that, an 8-bit radix
+      // select on ~id in shared memory finds the threshold thr (and how many
+      // keys equal to it to take: identical ids, outside the contract).
+      const uint32_t w2 = min(rinf, (uint32_t)ksel - nfin);
+      uint32_t thr = 0u, take_eq = 0u;  // every ~id is > 0: all of them when rinf == w2
+      if (w2 < rinf) {
+        uint32_t* hist = reinterpret_cast<uint32_t*>(s.live + nfin);  // 256 words after the list
+        uint32_t prefix = 0u, pmask = 0u, need = w2;
 #pragma unroll 1
-        for (int c0 = 0; c0 < n4; c0 += NT) {
-          const int c = c0 + tid;
-          uint32_t fm = 0u;
-          uint4 u4 = make_uint4(0u, 0u, 0u, 0u);
-          if (c < n4) {
-            const uint4 k4 = src.key4_global(t, c);
-            const uint4 i4 = src.ids4_global(t, c);
-            u4 = make_uint4(~i4.x, ~i4.y, ~i4.z, ~i4.w);
-            const uint32_t ks[4] = {k4.x, k4.y, k4.z, k4.w};
-            const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
+        for (int shift = 24; shift >= 0; shift -= 8) {
+          for (int i = tid; i < 256; i += NT) hist[i] = 0u;
+          row_sync();
+          for (uint32_t i = tid; i < rinf; i += NT) {
+            const uint32_t v = inf_ids[i];
+            if ((v & pmask) == prefix) atomicAdd(&hist[(v >> shift) & 0xFFu], 1u);
+          }
+          row_sync();
+          if (warp == 0) {
+            // lane l: digits 255 - 8l .. 248 - 8l, high to low
+            uint32_t h[8], local = 0u;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              bool in = ks[e] == kNegInfKey && us[e] != 0u;
-              if (in && select) {
-                const uint32_t um = us[e] & rr.mask;
-                // identical ids at the threshold (outside the contract): the
-                // first ones claimed fill the slots left
-                in = um > rr.prefix ||
-                     (um == rr.prefix && (rr.need == rr.count || atomicAdd(&sel.dup_claim, 1u) < rr.need));
+            for (int e = 0; e < 8; ++e) {
+              h[e] = hist[255 - 8 * lane - e];
+              local += h[e];
+            }
+            uint32_t above = warp_inclusive_scan(local) - local;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              if (h[e] != 0u && above < need && need <= above + h[e]) {
+                s.found_digit = (uint32_t)(255 - 8 * lane - e);
+                s.found_above = above;
               }
-              fm |= (in ? 1u : 0u) << e;
+              above += h[e];
             }
           }
-          const uint32_t cnt = __popc(fm);
-          const uint32_t incl = warp_inclusive_scan(cnt);
-          uint32_t base = 0u;
-          if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
-          uint32_t slot = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
-          const uint32_t us[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (fm & (1u << e)) {
-              if (slot < (uint32_t)kRowsLive)
-                s.live[slot] = ((unsigned long long)kNegInfKey << 32) | us[e];
-              ++slot;
-            }
-          }
+          row_sync();
+          prefix |= s.found_digit << shift;
+          pmask |= 0xFFu << shift;
+          need -= s.found_above;
+          row_sync();  // the scalars and the histogram are rewritten by the next pass
         }
+        thr = prefix;
+        take_eq = need;  // keys equal to thr to take (1 unless ids repeat)
+        if (tid == 0) s.lscal[7] = 0u;  // their claim counter (list_sort uses lscal[0..6])
         row_sync();
-        const uint32_t m2 = min(s.live_cursor, (uint32_t)kRowsLive);
+      }
+      // the -inf winners behind the finite keys: live[nfin, nfin + w2)
+      if (w2 > 0u) {
+        if (tid == 0) s.live_cursor = nfin;
+        row_sync();
+      }
+      for (uint32_t i0 = 0; w2 > 0u && i0 < rinf; i0 += NT) {
+        const uint32_t i = i0 + tid;
+        bool in = false;
+        uint32_t v = 0u;
+        if (i < rinf) {
+          v = inf_ids[i];
+          in = v > thr || (v == thr && atomicAdd(&s.lscal[7], 1u) < take_eq);
+        }
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, in);
+        uint32_t base = 0u;
+        if (lane == 0 && b) base = atomicAdd(&s.live_cursor, (uint32_t)__popc(b));
+        base = __shfl_sync(0xFFFFFFFFu, base, 0);
+        const uint32_t slot = base + __popc(b & ((1u << lane) - 1u));
+        if (in && slot < (uint32_t)kRowsLive) s.live[slot] = ((unsigned long long)kNegInfKey << 32) | v;
+      }
+      if (w2 > 0u) row_sync();
+      // the finite keys sorted to positions [0, nfin), the -inf winners to
+      // [nfin, nfin + w2) (list_sort's scratch reuses fine and region)
+      bool ok = list_sort<NT, 12, kRowsLive>(ls, (int)nfin, (int)nfin, out_at);
+      if (ok && w2 > 0u) {
+        ListScratch ls2 = ls;
+        ls2.list = s.live + nfin;
         off = (int)nfin;
-        ok = list_sort<NT, 12, kRowsLive>(ls, (int)m2, (int)min(w2, m2), out_at);
+        ok = list_sort<NT, 12, kRowsLive>(ls2, (int)w2, (int)w2, out_at);
       }
       if (ok) {
         for (int j = (int)(nfin + w2) + tid; j < ksel; j += NT) {
