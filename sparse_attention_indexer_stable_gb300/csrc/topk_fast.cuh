@@ -105,8 +105,11 @@ struct StreamShared {
   } u;
   uint32_t wa[kMaxWarps];
   uint32_t wb[kMaxWarps];
-  uint32_t stat_or[2];                // OR of the raw scores' bits below the bin; OR of ~ids (not 0)
-  uint32_t stat_and[2];               // [1]: AND of ~ids (not 0)
+  // per warp (plain stores, reduced where they are read: no same-address
+  // atomics from every warp)
+  uint32_t wraw[kMaxWarps];           // OR of the raw scores' bits below the bin
+  uint32_t wior[kMaxWarps];           // OR of ~ids (not 0)
+  uint32_t wiand[kMaxWarps];          // AND of ~ids (not 0)
   uint32_t live_cursor;
   uint32_t b1;                        // L1 bin of the K-th largest key
   uint32_t above_b1;                  // candidates in bins above b1
@@ -768,8 +771,6 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
     s.p_end = s.p_begin = 0u;
     s.overflow = 0u;
     s.pad_n = 0u;
-    s.stat_or[0] = s.stat_or[1] = 0u;
-    s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
   }
 
   // This CTA's rows are t = blockIdx.x + k * gridDim.x: walking the rows in
@@ -846,7 +847,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       }
     }
     raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & kLowMask);
-    if (lane == 0 && raw_or) atomicOr(&s.stat_or[0], raw_or);
+    if (lane == 0) s.wraw[warp] = raw_or;
     row_sync();
     // L1 was the last reader of the staged scores (the rest of the row works
     // from the keys in registers, the staged ids and, in the fallback, global
@@ -1010,8 +1011,8 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
         ior = __reduce_or_sync(0xFFFFFFFFu, ior);
         iand = __reduce_and_sync(0xFFFFFFFFu, iand);
         if (lane == 0) {
-          atomicOr(&s.stat_or[1], ior);
-          atomicAnd(&s.stat_and[1], iand);
+          s.wior[warp] = ior;
+          s.wiand[warp] = iand;
         }
       } else {
         // ids computed from the candidate index (below n): only the live
@@ -1041,10 +1042,13 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       // ordered like y = (low key bits >> tzf) << ibf | (~id low ibf bits), a
       // wf-bit number whose top q bits name the bucket.  Bins up to kPadBin
       // (-inf, where padding lives, and below) keep every bit.
-      const uint32_t ro = s.stat_or[0];
+      const uint32_t ro = __reduce_or_sync(0xFFFFFFFFu, lane < kWarpsT ? s.wraw[lane] : 0u);
       // ~id bits that vary: measured in COMPACT, or, for ids computed from
       // the candidate index i < n, the low bits of n - 1 (~i agrees above them)
-      const uint32_t vi = Source::kStagesIds ? s.stat_or[1] ^ s.stat_and[1]
+      const uint32_t vi = Source::kStagesIds
+                              ? __reduce_or_sync(0xFFFFFFFFu, lane < kWarpsT ? s.wior[lane] : 0u) ^
+                                    __reduce_and_sync(0xFFFFFFFFu,
+                                                      lane < kWarpsT ? s.wiand[lane] : 0xFFFFFFFFu)
                           : n > 1            ? 0xFFFFFFFFu >> __clz(n - 1)
                                              : 0u;
       const int tzf = ro ? min(__ffs(ro) - 1, kL1Shift) : kL1Shift;
@@ -1224,6 +1228,7 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       dbg_poison<NT>(s.fine, kFineMax + kL1Bins);
       dbg_poison<NT>(s.live, 2 * kLiveMax);
       dbg_poison<NT>(s.wa, 2 * kMaxWarps);
+      dbg_poison<NT>(s.wraw, 3 * kMaxWarps);
       if constexpr (!Source::kStagesIds) dbg_poison<NT>(aux, Caps::kScratchWords);
       if (tid == 0) {
         s.b1 = s.above_b1 = 0xA5A5A5A5u;
@@ -1239,8 +1244,6 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
       s.p_end = s.p_begin = 0u;
       s.overflow = 0u;
       s.pad_n = 0u;
-      s.stat_or[0] = s.stat_or[1] = 0u;
-      s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
     }
   }
 }

@@ -75,8 +75,9 @@ struct RowsShared {
   unsigned long long live[kRowsLive];  // live keys; the fallback's sorted winners
   uint32_t wa[kMaxWarps];
   uint32_t wb[kMaxWarps];              // SCAN1: window totals
-  uint32_t stat_or[2];                 // OR of the raw scores' bits below the bin; OR of live ~ids
-  uint32_t stat_and[2];                // [1]: AND of live ~ids (padding's 0 left out)
+  uint32_t wraw[kRowsNT / 32];         // per warp: OR of the raw scores' bits below the bin
+  uint32_t wior[kRowsNT / 32];         // per warp: OR of ~ids
+  uint32_t wiand[kRowsNT / 32];        // per warp: AND of ~ids (padding's 0 left out)
   uint32_t live_cursor;
   uint32_t b1;                         // L1 bin of the K-th largest key
   uint32_t nlive;                      // candidates in bins >= b1 (after refinement: live)
@@ -342,8 +343,6 @@ __global__ void __launch_bounds__(kRowsNT, 4)
     s.live_cursor = 0u;
     s.p_end = 0u;
     s.overflow = 0u;
-    s.stat_or[0] = s.stat_or[1] = 0u;
-    s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
   }
   const int G = (int)gridDim.x;
   int t = (int)blockIdx.x;
@@ -400,7 +399,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       }
     }
     raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & kLowMask);
-    if (lane == 0 && raw_or) atomicOr(&s.stat_or[0], raw_or);
+    if (lane == 0) s.wraw[warp] = raw_or;
     row_sync();
 
     // ---- SCAN1a: candidates per window of 128 bins (warp w: windows 4w..4w+3)
@@ -528,8 +527,8 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       ior = __reduce_or_sync(0xFFFFFFFFu, ior);
       iand = __reduce_and_sync(0xFFFFFFFFu, iand);
       if (lane == 0) {
-        atomicOr(&s.stat_or[1], ior);
-        atomicAnd(&s.stat_and[1], iand);
+        s.wior[warp] = ior;
+        s.wiand[warp] = iand;
       }
     }
     row_sync();
@@ -543,8 +542,9 @@ __global__ void __launch_bounds__(kRowsNT, 4)
     // buckets, name the bucket.  Bins up to kRowsPadBin (-inf, where padding
     // lives, and below) keep every bit.  Narrow rows (every live key above
     // that bin, wf <= 24) rank with 32-bit keys.
-    const uint32_t ro = s.stat_or[0];
-    const uint32_t vi = s.stat_or[1] ^ s.stat_and[1];
+    const uint32_t ro = __reduce_or_sync(0xFFFFFFFFu, lane < kWarpsT ? s.wraw[lane] : 0u);
+    const uint32_t vi = __reduce_or_sync(0xFFFFFFFFu, lane < kWarpsT ? s.wior[lane] : 0u) ^
+                        __reduce_and_sync(0xFFFFFFFFu, lane < kWarpsT ? s.wiand[lane] : 0xFFFFFFFFu);
     const int tzf = ro ? min(__ffs(ro) - 1, kL1Shift) : kL1Shift;
     const int ibf = vi ? 32 - __clz(vi) : 0;
     const uint32_t imask = ibf >= 32 ? 0xFFFFFFFFu : ((1u << ibf) - 1u);
@@ -762,7 +762,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         s.b1 = s.nlive = s.above_b1 = s.pad_cnt = s.pad_n = 0xA5A5A5A5u;
         s.found_digit = s.found_above = s.found_count = 0xA5A5A5A5u;
         s.live_cursor = s.p_end = s.overflow = 0xA5A5A5A5u;
-        s.stat_or[0] = s.stat_or[1] = s.stat_and[0] = s.stat_and[1] = 0xA5A5A5A5u;
+        for (int w = 0; w < kWarpsT; ++w) s.wraw[w] = s.wior[w] = s.wiand[w] = 0xA5A5A5A5u;
       }
       __syncthreads();
     }
@@ -771,8 +771,6 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       s.live_cursor = 0u;
       s.p_end = 0u;
       s.overflow = 0u;
-      s.stat_or[0] = s.stat_or[1] = 0u;
-      s.stat_and[0] = s.stat_and[1] = 0xFFFFFFFFu;
     }
   }
 }
