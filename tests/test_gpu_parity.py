@@ -247,6 +247,47 @@ def test_nans_and_padding(T):
     assert_same(run_merge(m), oracle.merge(m.scores, m.ids, m.row_starts), f"T={T}")
 
 
+def _neginf_rows(T, seed, dcp=4, K=2048):
+    """Rows whose K-th key is -inf, cycling over four shapes: every candidate
+    a real -inf; 1500 finite candidates and real -inf after them; real -inf
+    ids repeated across shards (outside the contract: identical keys, which
+    give identical outputs whichever is taken); finite, real -inf and padding
+    mixed."""
+    rng = np.random.default_rng(seed)
+    ids = workloads.distinct_ids(rng, dcp, T, K, 1 << 20)
+    scores = np.full((dcp, T, K), -np.inf, np.float32)
+    for t in range(T):
+        kind = t % 4
+        flat_s = scores[:, t, :].reshape(-1)
+        flat_i = ids[:, t, :].reshape(-1)
+        if kind == 1:
+            pos = rng.choice(dcp * K, 1500, replace=False)
+            flat_s[pos] = rng.standard_normal(1500).astype(np.float32)
+        elif kind == 2:
+            ids[1, t, :] = ids[0, t, :]
+            flat_i = ids[:, t, :].reshape(-1)
+            pos = rng.choice(dcp * K, 300, replace=False)
+            flat_s[pos] = rng.standard_normal(300).astype(np.float32)
+        elif kind == 3:
+            pos = rng.permutation(dcp * K)
+            flat_s[pos[:900]] = rng.standard_normal(900).astype(np.float32)
+            flat_i[pos[900 + 2500:]] = -1  # padding after 2500 real -inf candidates
+        scores[:, t, :] = flat_s.reshape(dcp, K)
+        ids[:, t, :] = flat_i.reshape(dcp, K)
+    return workloads.Merge("neginf-rows", scores, ids,
+                           rng.integers(0, 1 << 20, T).astype(np.int32))
+
+
+@pytest.mark.parametrize("T", [16, 160, 320])
+def test_neginf_threshold_rows(T):
+    """Rows whose winners include real -inf candidates chosen by id: the
+    split kernel (16 rows), the 512-thread kernel (160) and the many-row
+    kernel's shared-memory select on ~id (320)."""
+    m = _neginf_rows(T, seed=600 + T)
+    assert_same(run_merge(m), helpers.oracle_merge_all(m), f"T={T}")
+    assert dk.dcp_topk_device_status() == 0
+
+
 def test_all_padding_rows():
     dcp, T, K = 4, 3, 256
     scores = np.full((dcp, T, K), -np.inf, np.float32)
