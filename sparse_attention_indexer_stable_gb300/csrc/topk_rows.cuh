@@ -124,6 +124,7 @@ template <class Source>
 __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int t, int n,
                                            float* os, int32_t* oi) {
   constexpr int NT = kRowsNT;
+  constexpr int kWarpsT = NT / 32;
   constexpr int ksel = kRowsK;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n4 = n >> 2;
@@ -151,6 +152,7 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
     }
     row_sync();
     uint32_t npad = 0u;
+    uint32_t ior = 0u, iand = 0xFFFFFFFFu;  // over the real -inf candidates' ~ids
 #pragma unroll 1
     for (int c0 = 0; c0 < n4; c0 += NT) {
       const int c = c0 + tid;
@@ -167,8 +169,13 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
       for (int e = 0; e < 4; ++e) {
         if (c < n4) {
           fm |= (ks[e] > kNegInfKey ? 1u : 0u) << e;
-          im |= (ks[e] == kNegInfKey && us[e] != 0u ? 1u : 0u) << e;
+          const bool real_inf = ks[e] == kNegInfKey && us[e] != 0u;
+          im |= (real_inf ? 1u : 0u) << e;
           npad += (ks[e] == kNegInfKey && us[e] == 0u) ? 1u : 0u;
+          if (real_inf) {
+            ior |= us[e];
+            iand &= us[e];
+          }
         }
       }
       const uint32_t fcnt = __popc(fm);
@@ -199,7 +206,13 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
       }
     }
     npad = __reduce_add_sync(0xFFFFFFFFu, npad);
-    if (lane == 0 && npad != 0u) atomicAdd(&s.pad_n, npad);
+    ior = __reduce_or_sync(0xFFFFFFFFu, ior);
+    iand = __reduce_and_sync(0xFFFFFFFFu, iand);
+    if (lane == 0) {
+      if (npad != 0u) atomicAdd(&s.pad_n, npad);
+      s.wior[warp] = ior;  // the main path's slots, free here
+      s.wiand[warp] = iand;
+    }
     row_sync();
     const uint32_t nfin = s.live_cursor;                        // finite candidates
     const uint32_t rinf = min(s.found_count, (uint32_t)kRowsInfIds);  // real -inf candidates
@@ -213,9 +226,20 @@ __device__ __noinline__ void rows_fallback(const Source src, RowsShared& s, int 
       uint32_t thr = 0u, take_eq = 0u;  // every ~id is > 0: all of them when rinf == w2
       if (w2 < rinf) {
         uint32_t* hist = reinterpret_cast<uint32_t*>(s.live + nfin);  // 256 words after the list
+        // bits every real -inf ~id shares (ids from a narrow range share
+        // their top bits): digits made only of them are not histogrammed
+        const uint32_t all_and = __reduce_and_sync(
+            0xFFFFFFFFu, lane < kWarpsT ? s.wiand[lane] : 0xFFFFFFFFu);
+        const uint32_t varies =
+            __reduce_or_sync(0xFFFFFFFFu, lane < kWarpsT ? s.wior[lane] : 0u) ^ all_and;
         uint32_t prefix = 0u, pmask = 0u, need = w2;
 #pragma unroll 1
         for (int shift = 24; shift >= 0; shift -= 8) {
+          if (((varies >> shift) & 0xFFu) == 0u) {  // uniform: the digit every value has
+            prefix |= all_and & (0xFFu << shift);
+            pmask |= 0xFFu << shift;
+            continue;
+          }
           for (int i = tid; i < 256; i += NT) hist[i] = 0u;
           row_sync();
           for (uint32_t i = tid; i < rinf; i += NT) {
