@@ -10,7 +10,9 @@
 // 16-byte coalesced loads straight from the rank-major (dcp, T, K) buffers,
 // and the next row is prefetched into L2 about a third of a row ahead (early
 // enough to land, late enough to stay: a whole row ahead it was evicted again
-// and DRAM read 45% more than the candidates).
+// and DRAM read 45% more than the candidates).  The 32 score keys of a thread
+// wait in tensor memory from L1 to COMPACT, so the registers that held them
+// take the row's ids, loaded during SCAN1.
 //
 // Per row ("[Kernel] Optimize CuTeDSL DCP top-k merge", Summary: a radix pass
 // over 32-bit score keys first, the id tie-break only where scores tie):
@@ -88,6 +90,7 @@ struct RowsShared {
   uint32_t pad_cnt;                    // candidates in the -inf bin
   uint32_t pad_n;                      // fallback: padding candidates
   uint32_t lscal[8];                   // list_sort's scalars
+  uint32_t tmem_base;                  // this CTA's tensor-memory columns
 };
 static_assert(offsetof(RowsShared, region) == sizeof(uint32_t) * kRowsFine,
               "fine and the histogram are one region to reset");
@@ -103,6 +106,48 @@ static_assert(kRowsInfIds >= kRowsMaxN && 2 * (kRowsK - 1) + 256 <= 2 * kRowsLiv
 // Starts pulling `bytes` (a multiple of 16, 16-byte aligned) into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Tensor memory (TMEM) holds each thread's 32 score keys from L1 to COMPACT,
+// which frees the registers that hold them for the row's id loads (issued
+// right after L1, in flight through SCAN1).  A CTA allocates 64 columns once:
+// warp w owns columns 32*(w/4) .. +31 of lane quarter w%4 (a warp reaches
+// only its own quarter of the 128 lanes), one column per key.  Four CTAs per
+// SM take 256 of the 512 columns, so an allocation never waits on this
+// kernel's own CTAs (tcgen05.alloc blocks in hardware until columns are free;
+// a kernel of another stream holding TMEM on the SM can only delay it).
+__device__ __forceinline__ void tmem_alloc64(uint32_t* dst) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 64;\n"
+               ::"r"(smem_u32(dst)) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc64(uint32_t taddr) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 64;\n" ::"r"(taddr) : "memory");
+}
+// A CTA barrier that also orders tensor-memory operations around it.
+__device__ __forceinline__ void tmem_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+// r[0..32) into columns taddr .. taddr+31 of the thread's lane; returns once
+// the store has completed (the registers are free again).
+__device__ __forceinline__ void tmem_store32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n"
+      "tcgen05.wait::st.sync.aligned;\n"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+// Columns taddr .. taddr+7 of the thread's lane into r, waited for.
+__device__ __forceinline__ void tmem_load8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
 }
 
 __device__ __forceinline__ uint4 ldg4(const void* p) {
@@ -379,6 +424,10 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       return;
     }
   }
+  if (warp == 0) tmem_alloc64(&s.tmem_base);
+  tmem_sync();
+  const uint32_t tkeys =
+      s.tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(32 * (warp >> 2));
   if (tid == 0 && t < T) src.prefetch_row(t);
 
   for (; t < T; t += G) {
@@ -424,6 +473,15 @@ __global__ void __launch_bounds__(kRowsNT, 4)
     }
     raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & kLowMask);
     if (lane == 0) s.wraw[warp] = raw_or;
+    // the keys to tensor memory; the row's ids into the registers they held,
+    // in flight through SCAN1 (chunk v exists for v < nv = 2*dcp >= 2,
+    // uniform across the CTA; the loads take addresses clamped into the row,
+    // so none waits behind a branch)
+    tmem_store32(tkeys, keys);
+    const int nv = (n4 - tid + NT - 1) / NT;
+    uint4 ivs[kVec];
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) ivs[v] = ldg4(id_chunk(v < nv ? v : nv - 1));
     row_sync();
 
     // ---- SCAN1a: candidates per window of 128 bins (warp w: windows 4w..4w+3)
@@ -481,9 +539,15 @@ __global__ void __launch_bounds__(kRowsNT, 4)
     uint32_t live_from = b1 << 11;
     if (s.nlive > (uint32_t)kRowsLive) {
 #pragma unroll
-      for (int j = 0; j < kItems; ++j) {
-        if ((tid + (j >> 2) * NT) < n4 && (keys[j] >> kL1Shift) == b1)
-          atomicAdd(&s.fine[(keys[j] >> kRefShift) & 0x7FFu], 1u);
+      for (int c = 0; c < kItems / 8; ++c) {
+        uint32_t kc[8];
+        tmem_load8(tkeys + 8 * c, kc);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = 8 * c + e;
+          if ((tid + (j >> 2) * NT) < n4 && (kc[e] >> kL1Shift) == b1)
+            atomicAdd(&s.fine[(kc[e] >> kRefShift) & 0x7FFu], 1u);
+        }
       }
       row_sync();
       find_digit_desc<NT>(s.fine, (uint32_t)ksel - s.above_b1, s.wa, s.wb, s.found_digit,
@@ -516,7 +580,12 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       if (lf != 0u) {
         // candidates past the row hold key 0 (< lf)
 #pragma unroll
-        for (int j = 0; j < kItems; ++j) mask |= (keys[j] >= lf ? 1u : 0u) << j;
+        for (int c = 0; c < kItems / 8; ++c) {
+          uint32_t kc[8];
+          tmem_load8(tkeys + 8 * c, kc);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mask |= (kc[e] >= lf ? 1u : 0u) << (8 * c + e);
+        }
       } else {
 #pragma unroll
         for (int j = 0; j < kItems; ++j) mask |= ((tid + (j >> 2) * NT) < n4 ? 1u : 0u) << j;
@@ -531,10 +600,12 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       // is the smallest, so ordering on the varying bits alone still puts
       // it last)
       uint32_t ior = 0u, iand = 0xFFFFFFFFu;
+      uint32_t kc[8];  // the keys of chunks v and v+1, from tensor memory
 #pragma unroll
       for (int v = 0; v < kVec; ++v) {
-        if ((tid + v * NT) < n4) {
-          const uint4 iv = ldg4(id_chunk(v));
+        if ((v & 1) == 0) tmem_load8(tkeys + 4 * v, kc);
+        if (v < nv) {
+          const uint4 iv = ivs[v];
           const uint32_t us[4] = {~iv.x, ~iv.y, ~iv.z, ~iv.w};
           ior |= us[0] | us[1] | us[2] | us[3];
           if (has_pad)
@@ -545,7 +616,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             if (mask & (1u << (4 * v + e)))
-              *dst++ = ((unsigned long long)keys[4 * v + e] << 32) | us[e];
+              *dst++ = ((unsigned long long)kc[4 * (v & 1) + e] << 32) | us[e];
         }
       }
       ior = __reduce_or_sync(0xFFFFFFFFu, ior);
@@ -797,6 +868,8 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       s.overflow = 0u;
     }
   }
+  tmem_sync();  // every warp's last tensor-memory access is done
+  if (warp == 0) tmem_dealloc64(s.tmem_base);
 }
 
 }  // namespace dcp
