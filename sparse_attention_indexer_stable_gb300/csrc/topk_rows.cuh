@@ -393,12 +393,15 @@ __global__ void __launch_bounds__(kRowsNT, 4)
   extern __shared__ __align__(16) unsigned char smem_raw[];
   RowsShared& s = *reinterpret_cast<RowsShared*>(smem_raw);
   uint32_t* table = s.region;
-  // RANK's scratch in the region (free after L2): wide rows 64-bit rank keys,
-  // narrow rows 32-bit rank keys and list indices; bucket info for both.
+  // RANK's scratch in the region (free after L2): wide rows 64-bit rank keys
+  // (with the list index) and 16-bit bucket info; narrow rows 32-bit rank
+  // keys and 32-bit bucket info that also holds the L1 bin, from which RANK
+  // rebuilds a winner's key and ~id without going back to the list.
   unsigned long long* rk64 = reinterpret_cast<unsigned long long*>(s.region);
   uint32_t* rk32 = s.region;
-  uint16_t* pidx = reinterpret_cast<uint16_t*>(s.region + kRowsRankMax + 8);
+  uint32_t* info32 = s.region + kRowsRankMax + 8;  // bin << 16 | size << 8 | slot
   uint16_t* info = reinterpret_cast<uint16_t*>(s.region + kRowsRankWords);
+  static_assert(2 * (kRowsRankMax + 8) <= kRowsRegionWords, "narrow RANK scratch");
   const int n = src.count();  // dcp * 2048
   const int n4 = n >> 2;
   const int tid = threadIdx.x;
@@ -596,9 +599,11 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
       unsigned long long* dst =
           s.live + dbg_clamp(__shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt, kRowsLive + 1u - cnt);
-      // OR / AND of the row's inverted ids (padding's ~id of 0 left out: it
-      // is the smallest, so ordering on the varying bits alone still puts
-      // it last)
+      // OR / AND of the row's inverted ids.  Padding (a -inf key with the
+      // ~id 0) is left out of the AND: it is the smallest, so ordering on
+      // the varying bits alone still puts it last.  Every other candidate
+      // counts, so a narrow row's winners are their ~id bits under imask
+      // over the bits all of them share (RANK rebuilds the ids that way).
       uint32_t ior = 0u, iand = 0xFFFFFFFFu;
       uint32_t kc[8];  // the keys of chunks v and v+1, from tensor memory
 #pragma unroll
@@ -608,9 +613,11 @@ __global__ void __launch_bounds__(kRowsNT, 4)
           const uint4 iv = ivs[v];
           const uint32_t us[4] = {~iv.x, ~iv.y, ~iv.z, ~iv.w};
           ior |= us[0] | us[1] | us[2] | us[3];
-          if (has_pad)
-            iand &= (us[0] ? us[0] : 0xFFFFFFFFu) & (us[1] ? us[1] : 0xFFFFFFFFu) &
-                    (us[2] ? us[2] : 0xFFFFFFFFu) & (us[3] ? us[3] : 0xFFFFFFFFu);
+          if (has_pad) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              iand &= (us[e] == 0u && kc[4 * (v & 1) + e] == kNegInfKey) ? 0xFFFFFFFFu : us[e];
+          }
           else
             iand &= us[0] & us[1] & us[2] & us[3];
 #pragma unroll
@@ -763,10 +770,9 @@ __global__ void __launch_bounds__(kRowsNT, 4)
           if ((old >> 16) < (uint32_t)ksel) {
             const uint32_t pos = dbg_clamp((old >> 16) + (old & 0xFFu), kRowsRankMax);
             const uint32_t e = (uint32_t)(tid + u * NT);
-            info[pos] = (uint16_t)(old & 0xFFFFu);
-            pidx[pos] = (uint16_t)e;
             const unsigned long long lk = s.live[e];
             const uint32_t kk = (uint32_t)(lk >> 32);
+            info32[pos] = (old & 0xFFFFu) | ((kk >> kL1Shift) << 16);
             const uint32_t y = (((kk & kLowMask) >> tzf) << ibf) | ((uint32_t)lk & imask);
             rk32[pos] = (y << 8) | (255u - (old & 0xFFu));
           }
@@ -775,10 +781,16 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       row_sync();
       // ---- RANK: position = bucket start + members ranking above ---------
       const uint32_t p_end = min(s.p_end, (uint32_t)kRowsRankMax);
+      // a winner's key and ~id from its bin and y: the key bits below tzf
+      // are those of its sign (0 for positive scores, 1 for negative), the
+      // ~id bits above ibf those every candidate but padding shares
+      const uint32_t tzfill = (1u << tzf) - 1u;
+      const uint32_t ihigh = __reduce_and_sync(
+          0xFFFFFFFFu, lane < kWarpsT ? s.wiand[lane] : 0xFFFFFFFFu) & ~imask;
       for (uint32_t p = tid; p < p_end; p += NT) {
-        const uint32_t inf = info[p];
+        const uint32_t inf = info32[p];
         const uint32_t st = dbg_clamp(p - (inf & 0xFFu), p + 1u);
-        const uint32_t cnt = dbg_clamp(inf >> 8, kRowsRankMax + 9u - st);
+        const uint32_t cnt = dbg_clamp((inf >> 8) & 0xFFu, kRowsRankMax + 9u - st);
         const uint32_t mine = rk32[p];
         const uint32_t mc = __reduce_max_sync(__activemask(), cnt);
         uint32_t r = 0u;
@@ -796,9 +808,11 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         }
         const uint32_t fin = st + r;
         if (fin < (uint32_t)ksel) {
-          const unsigned long long key = s.live[dbg_clamp(pidx[p], kRowsLive)];
-          os[fin] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
-          oi[fin] = src.out_id_from(rbase, (uint32_t)key);
+          const uint32_t bin = inf >> 16;
+          const uint32_t y = mine >> 8;
+          const uint32_t kk = (bin << kL1Shift) | ((y >> ibf) << tzf) | (bin >= 0x800u ? 0u : tzfill);
+          os[fin] = __uint_as_float(score_bits(kk));
+          oi[fin] = src.out_id_from(rbase, (y & imask) | ihigh);
         }
       }
     } else if (fast) {
