@@ -23,9 +23,9 @@
 //           of candidates in higher bins, and count(b).  The bin b1 with
 //           above(b1) < K <= above(b1) + count(b1) holds the K-th key.
 //  COMPACT  candidates of bins >= b1 ("live", about K + a part of b1) are
-//           packed as 64-bit keys score_key << 32 | ~id; the ids are read
-//           here.  A bin b1 too full for the list is refined first on its
-//           next 11 key bits.
+//           packed as 64-bit entries score_key << 32 | id (the id inverted
+//           where it is used); the ids were loaded during SCAN1.  A bin b1
+//           too full for the list is refined first on its next 11 key bits.
 //  L2       buckets in position space: bin b owns buckets
 //           [above(b), above(b) + count(b)), one per candidate, and each live
 //           key goes to the bucket named by the top bits of its key below the
@@ -477,14 +477,12 @@ __global__ void __launch_bounds__(kRowsNT, 4)
     raw_or = __reduce_or_sync(0xFFFFFFFFu, raw_or & kLowMask);
     if (lane == 0) s.wraw[warp] = raw_or;
     // the keys to tensor memory; the row's ids into the registers they held,
-    // in flight through SCAN1 (chunk v exists for v < nv = 2*dcp >= 2,
-    // uniform across the CTA; the loads take addresses clamped into the row,
-    // so none waits behind a branch)
+    // in flight through SCAN1 (predicated loads, none behind a branch)
     tmem_store32(tkeys, keys);
-    const int nv = (n4 - tid + NT - 1) / NT;
     uint4 ivs[kVec];
 #pragma unroll
-    for (int v = 0; v < kVec; ++v) ivs[v] = ldg4(id_chunk(v < nv ? v : nv - 1));
+    for (int v = 0; v < kVec; ++v)
+      ivs[v] = (tid + v * NT) < n4 ? ldg4(id_chunk(v)) : make_uint4(0u, 0u, 0u, 0u);
     row_sync();
 
     // ---- SCAN1a: candidates per window of 128 bins (warp w: windows 4w..4w+3)
@@ -599,35 +597,36 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       if (lane == 31) base = atomicAdd(&s.live_cursor, incl);
       unsigned long long* dst =
           s.live + dbg_clamp(__shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt, kRowsLive + 1u - cnt);
-      // OR / AND of the row's inverted ids.  Padding (a -inf key with the
-      // ~id 0) is left out of the AND: it is the smallest, so ordering on
-      // the varying bits alone still puts it last.  Every other candidate
-      // counts, so a narrow row's winners are their ~id bits under imask
-      // over the bits all of them share (RANK rebuilds the ids that way).
-      uint32_t ior = 0u, iand = 0xFFFFFFFFu;
+      // OR / AND of the row's inverted ids, taken as the AND / OR of the raw
+      // ids.  Padding (a -inf key with the id -1) is left out of the OR: its
+      // ~id of 0 is the smallest, so ordering on the varying bits alone still
+      // puts it last.  Every other candidate counts, so a narrow row's
+      // winners are their ~id bits under imask over the bits all of them
+      // share (RANK rebuilds the ids that way).  The list holds the raw ids.
+      uint32_t rand_ = 0xFFFFFFFFu, ror = 0u;  // AND / OR of the raw ids
       uint32_t kc[8];  // the keys of chunks v and v+1, from tensor memory
 #pragma unroll
       for (int v = 0; v < kVec; ++v) {
         if ((v & 1) == 0) tmem_load8(tkeys + 4 * v, kc);
-        if (v < nv) {
+        if ((tid + v * NT) < n4) {
           const uint4 iv = ivs[v];
-          const uint32_t us[4] = {~iv.x, ~iv.y, ~iv.z, ~iv.w};
-          ior |= us[0] | us[1] | us[2] | us[3];
+          const uint32_t us[4] = {iv.x, iv.y, iv.z, iv.w};
+          rand_ &= us[0] & us[1] & us[2] & us[3];
           if (has_pad) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              iand &= (us[e] == 0u && kc[4 * (v & 1) + e] == kNegInfKey) ? 0xFFFFFFFFu : us[e];
+              ror |= (us[e] == 0xFFFFFFFFu && kc[4 * (v & 1) + e] == kNegInfKey) ? 0u : us[e];
           }
           else
-            iand &= us[0] & us[1] & us[2] & us[3];
+            ror |= us[0] | us[1] | us[2] | us[3];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             if (mask & (1u << (4 * v + e)))
               *dst++ = ((unsigned long long)kc[4 * (v & 1) + e] << 32) | us[e];
         }
       }
-      ior = __reduce_or_sync(0xFFFFFFFFu, ior);
-      iand = __reduce_and_sync(0xFFFFFFFFu, iand);
+      const uint32_t ior = ~__reduce_and_sync(0xFFFFFFFFu, rand_);
+      const uint32_t iand = ~__reduce_or_sync(0xFFFFFFFFu, ror);
       if (lane == 0) {
         s.wior[warp] = ior;
         s.wiand[warp] = iand;
@@ -663,7 +662,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
           const uint32_t kk = (uint32_t)(lk >> 32);
           const uint32_t tb = table[kk >> kL1Shift];
           const int q = (int)(tb >> 25);
-          const uint32_t y = (((kk & kLowMask) >> tzf) << ibf) | ((uint32_t)lk & imask);
+          const uint32_t y = (((kk & kLowMask) >> tzf) << ibf) | (~(uint32_t)lk & imask);
           const int d = wf - q;
           const uint32_t sub = d >= 0 ? (y >> d) : (y << (-d));
           const uint32_t cb = (tb >> 11) & 0x3FFFu;
@@ -680,7 +679,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         if (e < nlive) {
           const unsigned long long lk = s.live[e];
           const uint32_t kk = (uint32_t)(lk >> 32);
-          const uint32_t inv = (uint32_t)lk;
+          const uint32_t inv = ~(uint32_t)lk;
           const uint32_t bin = kk >> kL1Shift;
           const uint32_t tb = table[bin];
           const int q = (int)(tb >> 25);
@@ -773,7 +772,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
             const unsigned long long lk = s.live[e];
             const uint32_t kk = (uint32_t)(lk >> 32);
             info32[pos] = (old & 0xFFFFu) | ((kk >> kL1Shift) << 16);
-            const uint32_t y = (((kk & kLowMask) >> tzf) << ibf) | ((uint32_t)lk & imask);
+            const uint32_t y = (((kk & kLowMask) >> tzf) << ibf) | (~(uint32_t)lk & imask);
             rk32[pos] = (y << 8) | (255u - (old & 0xFFu));
           }
         }
@@ -826,7 +825,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
             const uint32_t pos = dbg_clamp((old >> 16) + (old & 0xFFu), kRowsRankMax);
             const uint32_t e = (uint32_t)(tid + u * NT);
             info[pos] = (uint16_t)(old & 0xFFFFu);
-            rk64[pos] = (s.live[e] << 12) | e;
+            rk64[pos] = ((s.live[e] ^ 0xFFFFFFFFull) << 12) | e;
           }
         }
       }
@@ -856,7 +855,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
         if (fin < (uint32_t)ksel) {
           const unsigned long long key = s.live[dbg_clamp((uint32_t)mine & 0xFFFu, kRowsLive)];
           os[fin] = __uint_as_float(score_bits((uint32_t)(key >> 32)));
-          oi[fin] = src.out_id_from(rbase, (uint32_t)key);
+          oi[fin] = src.out_id_from(rbase, ~(uint32_t)key);
         }
       }
     } else {
