@@ -651,12 +651,11 @@ __global__ void __launch_bounds__(kRowsNT, 4)
     const uint32_t imask = ibf >= 32 ? 0xFFFFFFFFu : ((1u << ibf) - 1u);
     const int wf = kL1Shift - tzf + ibf;
     const bool narrow = b1 > kRowsPadBin && wf <= 24;
-    uint32_t gsl[kLivePer];
+    uint32_t gsl[kLivePer];  // wide rows: each list entry's bucket
     if (fast && narrow) {
 #pragma unroll
       for (int u = 0; u < kLivePer; ++u) {
         const int e = tid + u * NT;
-        gsl[u] = kNone;
         if (e < nlive) {
           const unsigned long long lk = s.live[e];
           const uint32_t kk = (uint32_t)(lk >> 32);
@@ -668,7 +667,9 @@ __global__ void __launch_bounds__(kRowsNT, 4)
           const uint32_t cb = (tb >> 11) & 0x3FFFu;
           const uint32_t g = dbg_clamp((tb & 0x7FFu) + cb - 1u - ((sub * cb) >> q), kRowsFine);
           atomicAdd(&s.fine[g], 1u);
-          gsl[u] = g;
+          // the entry becomes y << 32 | bin << 12 | bucket: SCATTER needs
+          // nothing else, and no bucket ids wait in registers across SCAN2
+          s.live[e] = ((unsigned long long)y << 32) | ((kk >> kL1Shift) << 12) | g;
         }
       }
     } else if (fast) {
@@ -764,16 +765,15 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       // share y's top bits, so y orders them, identical keys by their slot.
 #pragma unroll
       for (int u = 0; u < kLivePer; ++u) {
-        if (gsl[u] != kNone) {
-          const uint32_t old = atomicAdd(&s.fine[gsl[u]], 1u);
+        const int e = tid + u * NT;
+        if (e < nlive) {
+          const unsigned long long ent = s.live[e];
+          const uint32_t lo = (uint32_t)ent;
+          const uint32_t old = atomicAdd(&s.fine[dbg_clamp(lo & 0xFFFu, kRowsFine)], 1u);
           if ((old >> 16) < (uint32_t)ksel) {
             const uint32_t pos = dbg_clamp((old >> 16) + (old & 0xFFu), kRowsRankMax);
-            const uint32_t e = (uint32_t)(tid + u * NT);
-            const unsigned long long lk = s.live[e];
-            const uint32_t kk = (uint32_t)(lk >> 32);
-            info32[pos] = (old & 0xFFFFu) | ((kk >> kL1Shift) << 16);
-            const uint32_t y = (((kk & kLowMask) >> tzf) << ibf) | (~(uint32_t)lk & imask);
-            rk32[pos] = (y << 8) | (255u - (old & 0xFFu));
+            info32[pos] = (old & 0xFFFFu) | ((lo >> 12) << 16);
+            rk32[pos] = ((uint32_t)(ent >> 32) << 8) | (255u - (old & 0xFFu));
           }
         }
       }
