@@ -51,6 +51,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <type_traits>
 
 #include "topk_core.cuh"
 #include "topk_fast.cuh"
@@ -604,7 +605,10 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       // winners are their ~id bits under imask over the bits all of them
       // share (RANK rebuilds the ids that way).  The list holds the raw ids.
       uint32_t rand_ = 0xFFFFFFFFu, ror = 0u;  // AND / OR of the raw ids
-      uint32_t kc[8];  // the keys of chunks v and v+1, from tensor memory
+      // the loop in two copies, with and without padding in the row
+      auto compact_ids = [&](auto hp) {
+        constexpr bool HP = decltype(hp)::value;
+        uint32_t kc[8];  // the keys of chunks v and v+1, from tensor memory
 #pragma unroll
       for (int v = 0; v < kVec; ++v) {
         if ((v & 1) == 0) tmem_load8(tkeys + 4 * v, kc);
@@ -612,7 +616,7 @@ __global__ void __launch_bounds__(kRowsNT, 4)
           const uint4 iv = ivs[v];
           const uint32_t us[4] = {iv.x, iv.y, iv.z, iv.w};
           rand_ &= us[0] & us[1] & us[2] & us[3];
-          if (has_pad) {
+          if constexpr (HP) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               ror |= (us[e] == 0xFFFFFFFFu && kc[4 * (v & 1) + e] == kNegInfKey) ? 0u : us[e];
@@ -625,6 +629,11 @@ __global__ void __launch_bounds__(kRowsNT, 4)
               *dst++ = ((unsigned long long)kc[4 * (v & 1) + e] << 32) | us[e];
         }
       }
+      };
+      if (has_pad)
+        compact_ids(std::true_type{});
+      else
+        compact_ids(std::false_type{});
       const uint32_t ior = ~__reduce_and_sync(0xFFFFFFFFu, rand_);
       const uint32_t iand = ~__reduce_or_sync(0xFFFFFFFFu, ror);
       if (lane == 0) {
