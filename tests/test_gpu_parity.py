@@ -288,6 +288,49 @@ def test_neginf_threshold_rows(T):
     assert dk.dcp_topk_device_status() == 0
 
 
+def _finite_minus_one_rows(T, seed, dcp=4, K=2048):
+    """bf16-valued rows (the narrow bucket keys of the many-row merge) with
+    slots whose id is -1 but whose score is finite, cycling over four
+    shapes: a few such slots; such slots beside (-inf, -1) padding; every id
+    of the row -1 (finite scores); ids from a narrow offset range (so the ids'
+    top bits agree) with a few -1 slots.  Only (-inf, -1) is padding under
+    the contract; these rows check that the kernels, whose id statistics
+    leave padding out and which rebuild ids from the bits the row's ids
+    share, still give the oracle's bits."""
+    rng = np.random.default_rng(seed)
+    ids = workloads.distinct_ids(rng, dcp, T, K, 65536)
+    scores = workloads.round_to_bf16(rng.standard_normal((dcp, T, K)).astype(np.float32))
+    for t in range(T):
+        kind = t % 4
+        flat_s = scores[:, t, :].reshape(-1)
+        flat_i = ids[:, t, :].reshape(-1)
+        if kind == 0:
+            flat_i[rng.choice(dcp * K, 40, replace=False)] = -1
+        elif kind == 1:
+            pos = rng.permutation(dcp * K)
+            flat_i[pos[:30]] = -1
+            flat_s[pos[30:530]] = -np.inf
+            flat_i[pos[30:530]] = -1
+        elif kind == 2:
+            flat_i[:] = -1
+        else:
+            flat_i += 1 << 24
+            flat_i[rng.choice(dcp * K, 25, replace=False)] = -1
+        scores[:, t, :] = flat_s.reshape(dcp, K)
+        ids[:, t, :] = flat_i.reshape(dcp, K)
+    return workloads.Merge("finite-minus-one", scores, ids,
+                           rng.integers(0, 1 << 20, T).astype(np.int32))
+
+
+@pytest.mark.parametrize("T", [16, 160, 320])
+def test_finite_scores_with_id_minus_one(T):
+    """The split kernel (16 rows), the 512-thread kernel (160) and the
+    many-row merge (320) on rows holding finite-score slots with id -1."""
+    m = _finite_minus_one_rows(T, seed=700 + T)
+    assert_same(run_merge(m), helpers.oracle_merge_all(m), f"T={T}")
+    assert dk.dcp_topk_device_status() == 0
+
+
 def test_all_padding_rows():
     dcp, T, K = 4, 3, 256
     scores = np.full((dcp, T, K), -np.inf, np.float32)
