@@ -87,6 +87,12 @@ typedef enum {
  * persistent grid ("Reserve the sparse indexer's DCP top-k merge scratch
  * through the workspace manager", Purpose), and the result does not depend
  * on the chunking.
+ *
+ * On-chip resources: with K = 2048, dcp <= 4 and more than two rows per SM
+ * the kernel holds 64 tensor-memory columns per CTA (four CTAs, 256 of an
+ * SM's 512 columns) while it runs.  Its allocation waits in hardware for free
+ * columns, so a kernel on another stream that holds tensor memory on the same
+ * SM can delay it (and be delayed by it); neither waits on the other.
  */
 dcp_status dcp_topk_merge(const float* scores, const int32_t* ids, int T, int dcp, int K,
                           const int32_t* row_starts, int32_t* out_ids, float* out_scores,
