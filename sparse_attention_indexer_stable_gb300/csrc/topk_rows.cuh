@@ -805,6 +805,10 @@ __global__ void __launch_bounds__(kRowsNT, 4)
       const uint32_t tzfill = (1u << tzf) - 1u;
       const uint32_t ihigh = __reduce_and_sync(
           0xFFFFFFFFu, lane < kWarpsT ? s.wiand[lane] : 0xFFFFFFFFu) & ~imask;
+      // When every non-padding id is >= 0 (the usual case) their ~ids share
+      // bit 31, no winner is id -1, and the output needs no test for it.
+      auto rank_rows = [&](auto nonneg) {
+        constexpr bool NONNEG = decltype(nonneg)::value;
 #pragma unroll 2  // two positions per trip: measured 0.4% faster
       for (uint32_t p = tid; p < p_end; p += NT) {
         const uint32_t inf = info32[p];
@@ -831,9 +835,15 @@ __global__ void __launch_bounds__(kRowsNT, 4)
           const uint32_t y = mine >> 8;
           const uint32_t kk = (bin << kL1Shift) | ((y >> ibf) << tzf) | (bin >= 0x800u ? 0u : tzfill);
           os[fin] = __uint_as_float(score_bits(kk));
-          oi[fin] = src.out_id_from(rbase, (y & imask) | ihigh);
+          oi[fin] = NONNEG ? (int32_t)(rbase + ~((y & imask) | ihigh))
+                          : src.out_id_from(rbase, (y & imask) | ihigh);
         }
       }
+      };
+      if (ihigh >> 31)
+        rank_rows(std::true_type{});
+      else
+        rank_rows(std::false_type{});
     } else if (fast) {
       // ---- SCATTER: rank key (key without its L1 bin) << 12 | list index;
       // members of a bucket share their key's top 12 bits.
