@@ -299,13 +299,16 @@ __device__ __forceinline__ void find_digit_desc(const uint32_t* hist, uint32_t n
 // Shared-memory bytes of the streaming kernel with NT threads: the state, the
 // stage for a row's `score_words` scores, and the aux region (the row's
 // `ids_words` ids when they are staged, RANK's scratch after COMPACT; the
-// larger of the two).
+// larger of the two).  The stage and the aux region start on 128-byte
+// boundaries: bulk copies into a destination that was only 16-byte aligned
+// measured slower (decode merge 5.66 -> 5.60 us per launch, 5.41 -> 5.21 us
+// per graph replay; fused top-K of one row 6.58 -> 6.34 us).
 template <int NT, int KMAX = kStreamMaxK>
 inline size_t stream_smem_bytes(int score_words, int ids_words) {
   constexpr int kScratch = StreamCaps<NT, KMAX>::kScratchWords;
   const int aux = ids_words > kScratch ? ids_words : kScratch;
-  return ((sizeof(StreamSharedFor<NT, KMAX>) + 15) & ~(size_t)15) +
-         (size_t)((score_words + 3) & ~3) * 4 + (size_t)((aux + 3) & ~3) * 4;
+  return ((sizeof(StreamSharedFor<NT, KMAX>) + 127) & ~(size_t)127) +
+         (size_t)((score_words + 31) & ~31) * 4 + (size_t)((aux + 3) & ~3) * 4;
 }
 
 // Orders this thread's earlier shared-memory writes before later bulk copies
@@ -753,9 +756,9 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 2)
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Shared& s = *reinterpret_cast<Shared*>(smem_raw);
   uint32_t* stage =
-      reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(Shared) + 15) & ~(size_t)15));
+      reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(Shared) + 127) & ~(size_t)127));
   const int n = src.count();  // multiple of 4, <= MAXN
-  uint32_t* aux = stage + n;  // the row's ids (when staged), then RANK's scratch
+  uint32_t* aux = stage + ((n + 31) & ~31);  // the row's ids (when staged), then RANK's scratch
   unsigned long long* rkl = reinterpret_cast<unsigned long long*>(aux);
   uint16_t* info = reinterpret_cast<uint16_t*>(rkl + kRankMax);
   const int n4 = n >> 2;
